@@ -1,0 +1,242 @@
+/*
+ * libpadoc: ancestor-masked tree attention over a shared page-prefix KV cache.
+ *
+ * A page is a shared prefix X followed by a layout stream B_1..B_N and N
+ * content branches Y_1..Y_N.  Layout tokens attend causally to [X, B<=current];
+ * content tokens of Y_k attend to [X, B<=k] and to the earlier tokens of Y_k,
+ * and never to another branch (PaDoc, "Training paradigm": Anc(B_k) = {X, B<k},
+ * Anc(Y_k) = {X, B<=k}, realised as a packed tree-varlen attention).
+ *
+ * Conventions for every call:
+ *  - Return value: PADOC_OK (0) or a negative PADOC_ERR_* code.  On error,
+ *    padoc_last_error() returns a message (thread-local, valid until the next
+ *    call on the same thread).  No C++ exception crosses this boundary.
+ *  - Ownership: the caller owns every device buffer (Q, K, V, O, LSE, KV pool
+ *    storage, workspace) and the stream.  The library owns only the opaque
+ *    host handles it returns and a little device metadata that it allocates
+ *    outside the compute calls (descriptor upload, pool tables) and frees in
+ *    the matching *_free / *_destroy call.
+ *  - Compute calls enqueue work on `stream` and return without waiting.
+ *    Host calls are synchronous.  A handle may be used from one thread at a
+ *    time.
+ *  - "device pointer" means memory of the current CUDA device; "host pointer"
+ *    means ordinary CPU memory read during the call only.
+ *  - Kernel waits are bounded: a kernel that gives up on a wait records an
+ *    error that the next call on the same handle (or padoc_device_status)
+ *    reports as PADOC_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef PADOC_H_
+#define PADOC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PADOC_API __attribute__((visibility("default")))
+#else
+#define PADOC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* padoc_stream_t;
+
+enum {
+  PADOC_OK = 0,
+  PADOC_ERR_INVALID = -1,        /* bad argument or malformed structure; nothing changed */
+  PADOC_ERR_OOM = -2,            /* KV pool out of blocks or sequence slots; nothing changed */
+  PADOC_ERR_CUDA = -3,           /* a CUDA runtime call failed (message names it) */
+  PADOC_ERR_UNSUPPORTED = -4,    /* valid request this build does not implement */
+  PADOC_ERR_DEVICE_TIMEOUT = -5  /* a kernel gave up a bounded wait */
+};
+
+enum { PADOC_F32 = 0, PADOC_BF16 = 1 };
+
+/* Packing of one page's tokens in the packed (THD) token stream.  The pages
+ * fix no order; attention results per logical token do not depend on it. */
+enum {
+  PADOC_PACK_CANONICAL = 0, /* [X | B_1 .. B_N | Y_1 .. Y_N] */
+  PADOC_PACK_DOCUMENT = 1   /* [X | B_1 Y_1 | B_2 Y_2 | ...] */
+};
+
+PADOC_API const char* padoc_last_error(void);
+PADOC_API int padoc_version(void); /* major*10000 + minor*100 + patch */
+
+/* ------------------------------------------------------------------------
+ * Tree descriptor (host).  Turns region lengths into query segments, each
+ * with an ordered list of key/value segments, and a tile work list.
+ * Basis: PaDoc, "Training paradigm" (the layout stream is one causal
+ * sequence; Y_k queries attend to the virtual KV sequence [X, B<=k, Y_k]).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t n_pages;             /* >= 0 */
+  const int32_t* prefix_len;   /* host [n_pages], >= 0: tokens of X */
+  const int32_t* n_regions;    /* host [n_pages], >= 0: N */
+  const int32_t* layout_len;   /* host [sum n_regions], page-major, >= 0: l(B_k) */
+  const int32_t* content_len;  /* host [sum n_regions], page-major, >= 0: l(Y_k) (the
+                                  branch-start token counts as the first token of Y_k) */
+  int32_t order;               /* PADOC_PACK_* */
+} padoc_tree_spec;
+
+typedef struct padoc_tree_desc padoc_tree_desc;
+
+/* Builds the descriptor.  Pages are packed back to back in the given order;
+ * no page sees another.  Total tokens must stay below 2^31.
+ * Errors: PADOC_ERR_INVALID (negative length, bad order, overflow). */
+PADOC_API int padoc_tree_desc_build(const padoc_tree_spec* spec, padoc_tree_desc** out);
+PADOC_API int padoc_tree_desc_free(padoc_tree_desc* desc);
+
+/* Sizes: packed tokens, query segments, key/value segments, and the number
+ * of (query token, ancestor token) pairs (sum of ancestor-set sizes). */
+PADOC_API int padoc_tree_desc_info(const padoc_tree_desc* desc, int64_t* n_tokens, int64_t* n_qsegs,
+                         int64_t* n_kvsegs, int64_t* ancestor_pairs);
+
+/* Copies the segment lists out (for bit-exact checks).
+ *   qseg  host [n_qsegs][4]:  q_start, q_len, kv_first, kv_count
+ *   kvseg host [n_kvsegs][3]: kv_start, kv_len, causal
+ * A query at packed position t of segment s sees, for each of its key
+ * segments, positions [kv_start, kv_start + kv_len) when causal == 0 and
+ * [kv_start, min(kv_start + kv_len, t + 1)) when causal == 1. */
+PADOC_API int padoc_tree_desc_segments(const padoc_tree_desc* desc, int32_t* qseg, int32_t* kvseg);
+
+/* Allocates and fills the device copy of the descriptor for query-group size
+ * `group` = Hq / Hkv on the current device (synchronous).  The forward does
+ * this itself on first use; calling it first keeps allocation out of the
+ * first forward. */
+PADOC_API int padoc_tree_desc_upload(padoc_tree_desc* desc, int32_t group);
+
+/* ------------------------------------------------------------------------
+ * Packed tree-varlen forward (PaDoc, "Training paradigm"; tree-varlen).
+ *   q   device [T, Hq, d]   (THD, row-major, contiguous)
+ *   k,v device [T, Hkv, d]
+ *   o   device [T, Hq, d]   same dtype as q
+ *   lse device [Hq, T] f32  natural log of sum_j exp(scale * q.k_j) over the
+ *                           query's ancestor set
+ * dtype PADOC_BF16 (tensor-core path, f32 accumulation) or PADOC_F32 (f32
+ * CUDA-core path).  d must be 128 for bf16 and 64 or 128 for f32; Hq must
+ * be a multiple of Hkv with Hq / Hkv in {1, 2, 4, 8, 16}.  scale <= 0 means
+ * 1/sqrt(d).  Query head h reads kv head h / (Hq / Hkv).  Pointers must be
+ * 16-byte aligned.  T = 0 is a no-op. */
+PADOC_API int padoc_tree_attn_varlen(padoc_tree_desc* desc, const void* q, const void* k, const void* v,
+                           void* o, float* lse, int32_t dtype, int32_t Hq, int32_t Hkv,
+                           int32_t d, float scale, padoc_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Refcounted paged KV pool.  Storage is caller-owned device memory laid out
+ * [num_blocks, Hkv, block_size, d] for K and for V (one layer).  A sequence
+ * is a list of blocks; a fork shares the parent's blocks with zero copy and
+ * bumps their reference counts; release drops them and frees blocks that
+ * reach zero (HPD-Parsing: fork with zero-copy KV sharing and
+ * reference-counted release).
+ * ---------------------------------------------------------------------- */
+typedef struct padoc_kv_pool padoc_kv_pool;
+
+/* block_size must be 16; d must be 128; dtype PADOC_BF16.  max_seqs and
+ * max_blocks_per_seq size the device block table (allocated on first device
+ * use, see padoc_kv_pool_sync).  The environment variable
+ * PADOC_FAULT_ALLOC_AFTER=n makes the n-th later block allocation fail with
+ * PADOC_ERR_OOM (host fault injection for tests). */
+PADOC_API int padoc_kv_pool_create(padoc_kv_pool** out, void* k_pool, void* v_pool, int32_t num_blocks,
+                         int32_t block_size, int32_t Hkv, int32_t d, int32_t dtype,
+                         int32_t max_seqs, int32_t max_blocks_per_seq);
+PADOC_API int padoc_kv_pool_destroy(padoc_kv_pool* pool);
+
+/* New empty sequence with room reserved for n_tokens (>= 0) tokens.
+ * On PADOC_ERR_OOM nothing changes. */
+PADOC_API int padoc_kv_alloc(padoc_kv_pool* pool, int32_t n_tokens, int32_t* seq);
+
+/* Appends n tokens (device [n, Hkv, d] each for k and v, pool dtype) to the
+ * end of seq, growing it by fresh blocks if needed.  A forked sequence never
+ * writes into a shared block: its own tokens start in a fresh block.
+ * On PADOC_ERR_OOM nothing changes.  The copy runs on `stream`. */
+PADOC_API int padoc_kv_append(padoc_kv_pool* pool, int32_t seq, const void* k, const void* v, int32_t n,
+                    padoc_stream_t stream);
+
+/* New sequence whose first fork_len tokens are the parent's first fork_len
+ * tokens, shared with zero copy (the blocks covering them get refcount + 1,
+ * a partly used last block included).  0 <= fork_len <= length(parent). */
+PADOC_API int padoc_kv_fork(padoc_kv_pool* pool, int32_t parent, int32_t fork_len, int32_t* child);
+
+/* Drops the sequence: refcount - 1 on each of its blocks, blocks at 0 return
+ * to the free list, the sequence id becomes reusable. */
+PADOC_API int padoc_kv_release(padoc_kv_pool* pool, int32_t seq);
+
+/* Sequence facts: length, tokens shared from its fork parent, blocks held. */
+PADOC_API int padoc_kv_seq_info(const padoc_kv_pool* pool, int32_t seq, int32_t* length, int32_t* fork_len,
+                      int32_t* n_blocks);
+/* Copies the block ids of seq into out (host, capacity cap). */
+PADOC_API int padoc_kv_seq_blocks(const padoc_kv_pool* pool, int32_t seq, int32_t* out, int32_t cap);
+/* Reference count of one block (0 = free). */
+PADOC_API int padoc_kv_block_refcount(const padoc_kv_pool* pool, int32_t block, int32_t* refcount);
+/* Free blocks and live sequences. */
+PADOC_API int padoc_kv_pool_stats(const padoc_kv_pool* pool, int32_t* free_blocks, int32_t* live_seqs);
+/* Allocates the device block table if needed and uploads changed rows
+ * (synchronous with respect to the host tables; copies enqueue on stream). */
+PADOC_API int padoc_kv_pool_sync(padoc_kv_pool* pool, padoc_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Branch-parallel decode and speculative verify over the pool.
+ * Every live branch queries 1..16 tokens against the shared prefix of its
+ * page plus its own cached suffix; inside the query block each token sees
+ * its draft-tree ancestors and itself (HSD page, "prefix-tree batching";
+ * HPD-Parsing: parallel verify of drafted tokens on forked branches).
+ * The shared prefix of a page is streamed from HBM once for all branches of
+ * the page (cascade); partial softmaxes are merged by log-sum-exp.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t n_pages;
+  int32_t n_branches;
+  const int32_t* page_seq;       /* host [n_pages]: sequence holding the page's shared prefix */
+  const int32_t* branch_offsets; /* host [n_pages + 1]: page p owns branches
+                                    [branch_offsets[p], branch_offsets[p+1]) */
+  const int32_t* branch_seq;     /* host [n_branches]: the branch's sequence, a fork of its
+                                    page's sequence; it sees the fork_len shared tokens as its
+                                    prefix and the rest of its tokens as its own suffix */
+  const int32_t* q_offsets;      /* host [n_branches + 1]: query rows of branch b are
+                                    [q_offsets[b], q_offsets[b+1]), between 1 and 16 */
+} padoc_decode_batch;
+
+/* Workspace bytes padoc_branch_decode needs for this batch and head count. */
+PADOC_API int padoc_branch_decode_ws_size(const padoc_kv_pool* pool, const padoc_decode_batch* batch,
+                                int32_t Hq, size_t* bytes);
+
+/*   q         device [nq, Hq, d] pool dtype; nq = q_offsets[n_branches]
+ *   k_new     device [nq, Hkv, d]: keys of the step's own query tokens (not yet in the
+ *   v_new               cache; commit accepted ones later with padoc_kv_append)
+ *   tree_bits device [nq] uint16 or NULL: bit j of row i (within its branch) set iff
+ *             query token j of the same branch is visible to token i; NULL means a chain
+ *             (j <= i).  Bit i must be set for every row.  padoc_tree_mask_build fills it
+ *             from a parent array.
+ *   o         device [nq, Hq, d] pool dtype
+ *   lse       device [nq, Hq] f32, natural log
+ *   ws        device workspace of at least padoc_branch_decode_ws_size bytes, 256-byte
+ *             aligned, not shared with a call still running
+ * Hq must be a multiple of the pool's Hkv with Hq / Hkv <= 8.  scale <= 0 means
+ * 1/sqrt(d).  Validation happens on the host before any launch. */
+PADOC_API int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq,
+                        const void* q, const void* k_new, const void* v_new,
+                        const uint16_t* tree_bits, void* o, float* lse, float scale, void* ws,
+                        size_t ws_bytes, padoc_stream_t stream);
+
+/* Draft-tree visibility (HSD page, "prefix-tree batching"): for n <= 16 nodes
+ * in topological order (parent[i] < i, -1 for a root), bits[i] gets bit j set
+ * iff node j is node i or one of its ancestors.  Host arrays. */
+PADOC_API int padoc_tree_mask_build(const int32_t* parent, int32_t n, uint16_t* bits);
+
+/* Critical-path depths of one page (PaDoc, theoretical speedup):
+ * d_seq = l(B_1:N) + sum_k l(Y_k);  d_tree = max_k [l(B<=k) + l(Y_k)]. */
+PADOC_API int padoc_depths(const int32_t* layout_len, const int32_t* content_len, int32_t n_regions,
+                 int64_t* d_seq, int64_t* d_tree);
+
+/* Reports and clears the device error word of the current device: 0 when no
+ * kernel has given up a wait since the last call, else PADOC_ERR_DEVICE_TIMEOUT
+ * with the failing site in the message. */
+PADOC_API int padoc_device_status(padoc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PADOC_H_ */

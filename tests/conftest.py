@@ -28,3 +28,11 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def padoc_lib():
+    """Builds (if stale) and loads libpadoc.so."""
+    from tree_structured_shared_gb300 import build, padoc
+    build.build()
+    return padoc.lib()

@@ -1,0 +1,181 @@
+"""C-ABI checks that need no GPU: exported symbols, the tree-descriptor
+builder (bit-exact against the oracle's ancestor sets), the draft-tree mask
+and depth helpers, and the KV pool's host bookkeeping."""
+import os
+import re
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+from oracle import tree_attention as ta
+from tree_structured_shared_gb300 import padoc
+from tree_structured_shared_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_exports_every_declared_symbol(padoc_lib):
+    hdr = open(os.path.join(ROOT, "include", "padoc.h")).read()
+    declared = set(re.findall(r"PADOC_API\s+[\w\s\*]+?\b(padoc_\w+)\s*\(", hdr))
+    assert len(declared) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", padoc.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(padoc_\w+)", out))
+    assert declared <= exported, declared - exported
+    assert set(padoc.EXPORTED) == declared
+    assert padoc_lib.padoc_version() == 100
+
+
+def _expand(qs, kv, T):
+    """Per-token visible key runs from the descriptor's segment lists."""
+    runs = [None] * T
+    for q_start, q_len, kv_first, kv_count in qs:
+        for t in range(q_start, q_start + q_len):
+            r = []
+            for s in range(kv_first, kv_first + kv_count):
+                a, n, causal = kv[s]
+                b = min(a + n, t + 1) if causal else a + n
+                if b > a:
+                    if r and r[-1][1] == a:
+                        r[-1] = (r[-1][0], b)
+                    else:
+                        r.append((a, b))
+            assert runs[t] is None, "token covered twice"
+            runs[t] = r
+    return runs
+
+
+@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("order", [padoc.PACK_CANONICAL, padoc.PACK_DOCUMENT])
+def test_descriptor_matches_oracle_ancestors(padoc_lib, seed, order):
+    w = wl.random_pages(seed, n_pages=4, max_prefix=30, max_regions=6, max_layout=5, max_content=25)
+    desc = padoc.TreeDesc(w.pages, order)
+    inf = desc.info()
+    assert inf["n_tokens"] == w.n_tokens
+    qs, kv = desc.segments()
+    got = _expand(qs, kv, w.n_tokens)
+    want = ta.segment_intervals(w.pages, order)
+    assert got == [list(x) for x in want]
+    assert inf["ancestor_pairs"] == sum(len(a) for a in ta.ancestor_positions(w.pages, order))
+
+
+def test_descriptor_config_shapes(padoc_lib):
+    for w in (wl.tiny_fp32_page(0), wl.qwen_page(0)):
+        desc = padoc.TreeDesc(w.pages)
+        qs, kv = desc.segments()
+        # canonical packing: one causal layout stream plus one segment per content branch
+        assert len(qs) == 1 + sum(1 for c in w.pages[0].content_len if c > 0)
+        assert max(qs[:, 3]) <= 2
+        got = _expand(qs, kv, w.n_tokens)
+        want = ta.segment_intervals(w.pages)
+        assert got == [list(x) for x in want]
+
+
+def test_descriptor_rejects_bad_input(padoc_lib):
+    with pytest.raises(padoc.PadocError) as e:
+        padoc.TreeDesc([wl.Page(-1, [], [])])
+    assert e.value.code == padoc.ERR_INVALID
+    with pytest.raises(padoc.PadocError):
+        padoc.TreeDesc([wl.Page(3, [2], [-4])])
+    with pytest.raises(padoc.PadocError):
+        padoc.TreeDesc([wl.Page(3, [], [])], order=7)
+    d = padoc.TreeDesc([])
+    assert d.info()["n_tokens"] == 0
+
+
+def test_tree_mask_build_matches_oracle(padoc_lib):
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        par = wl.draft_tree(rng)
+        if len(par) > 2 and rng.random() < 0.3:
+            par[int(rng.integers(1, len(par)))] = -1
+        assert list(padoc.tree_mask_build(par)) == ta.tree_mask_bits(par)
+    with pytest.raises(padoc.PadocError):
+        padoc.tree_mask_build([0])       # a node cannot be its own parent
+    with pytest.raises(padoc.PadocError):
+        padoc.tree_mask_build([-1] * 17)  # more than 16 nodes
+
+
+def test_depths_match_oracle(padoc_lib):
+    rng = np.random.default_rng(1)
+    for _ in range(100):
+        n = int(rng.integers(0, 30))
+        lay = rng.integers(0, 20, n).tolist()
+        con = rng.integers(0, 200, n).tolist()
+        assert padoc.depths(lay, con) == ta.depths(lay, con)
+
+
+# ---------------------------------------------------------------- KV pool (host bookkeeping)
+
+
+def _pool(nb=64, max_seqs=16, max_bps=16):
+    return padoc.KVPool(None, None, nb, Hkv=2, d=128, max_seqs=max_seqs, max_blocks_per_seq=max_bps)
+
+
+def test_pool_alloc_fork_release_refcounts(padoc_lib):
+    pool = _pool()
+    a = pool.alloc(40)  # 3 blocks reserved, length 0
+    assert pool.seq_info(a) == {"length": 0, "fork_len": 0, "n_blocks": 3}
+    assert pool.stats() == {"free_blocks": 61, "live_seqs": 1}
+    blocks = pool.seq_blocks(a)
+    assert all(pool.refcount(b) == 1 for b in blocks)
+    with pytest.raises(padoc.PadocError):
+        pool.fork(a, 1)  # fork beyond the parent's length
+    c = pool.fork(a, 0)
+    assert pool.seq_info(c)["n_blocks"] == 0
+    pool.release(c)
+    assert pool.stats()["live_seqs"] == 1
+    pool.release(a)
+    assert pool.stats() == {"free_blocks": 64, "live_seqs": 0}
+    assert all(pool.refcount(b) == 0 for b in blocks)
+    with pytest.raises(padoc.PadocError):
+        pool.release(a)
+
+
+def test_pool_oom_changes_nothing(padoc_lib):
+    pool = _pool(nb=8, max_seqs=4)
+    a = pool.alloc(100)  # 7 blocks
+    before = pool.stats()
+    with pytest.raises(padoc.PadocError) as e:
+        pool.alloc(33)   # 3 blocks, only 1 left
+    assert e.value.code == padoc.ERR_OOM
+    assert pool.stats() == before
+    pool.alloc(16)
+    pool.alloc(0)
+    pool.alloc(0)
+    with pytest.raises(padoc.PadocError) as e:
+        pool.alloc(0)    # no sequence slot left
+    assert e.value.code == padoc.ERR_OOM
+    pool.release(a)
+
+
+def test_pool_fault_injection_after_n_blocks(padoc_lib):
+    code = (
+        "import os, sys; sys.path.insert(0, %r)\n"
+        "from tree_structured_shared_gb300 import padoc\n"
+        "pool = padoc.KVPool(None, None, 64, Hkv=2, d=128, max_seqs=8, max_blocks_per_seq=16)\n"
+        "a = pool.alloc(48)\n"
+        "s0 = pool.stats()\n"
+        "try:\n"
+        "    pool.alloc(32)\n"
+        "    print('NOFAULT')\n"
+        "except padoc.PadocError as e:\n"
+        "    print('FAULT', e.code, pool.stats() == s0, pool.seq_info(a)['n_blocks'])\n"
+    ) % ROOT
+    env = dict(os.environ, PADOC_FAULT_ALLOC_AFTER="4")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+    assert out.stdout.strip() == "FAULT -2 True 3", out.stdout + out.stderr
+
+
+def test_pool_rejects_bad_arguments(padoc_lib):
+    with pytest.raises(padoc.PadocError) as e:
+        padoc.KVPool(None, None, 8, Hkv=2, d=64)
+    assert e.value.code == padoc.ERR_UNSUPPORTED
+    with pytest.raises(padoc.PadocError):
+        padoc.KVPool(None, None, 0, Hkv=2, d=128)
+    pool = _pool(max_bps=2)
+    with pytest.raises(padoc.PadocError):
+        pool.alloc(33)  # 3 blocks > max_blocks_per_seq
+    with pytest.raises(padoc.PadocError):
+        pool.seq_info(5)

@@ -1,0 +1,116 @@
+"""Branch decode / speculative verify on the GPU against the float64 oracle."""
+import numpy as np
+import pytest
+
+from oracle import tree_attention as ta
+from tree_structured_shared_gb300 import padoc
+from tree_structured_shared_gb300 import workloads as wl
+
+from parity import check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def harness(padoc_lib):
+    from tree_structured_shared_gb300 import harness as h
+    return h
+
+
+def _decode(harness, w, seed=0, tree=True):
+    import torch
+    vals = wl.decode_values(w, seed)
+    d = harness.Decode(w, vals, tree=tree)
+    o, lse = d.run()
+    torch.cuda.synchronize()
+    padoc.device_status()
+    O, L = ta.branch_decode(w, vals, tree=tree)
+    return o.float().cpu().numpy()[: w.n_queries], lse.cpu().numpy()[: w.n_queries], O, L
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_small_verify_ragged(harness, seed):
+    """Draft trees and forests, empty own suffixes, per-branch prefix lengths
+    below the page prefix, G = 2."""
+    w = wl.small_decode(seed, n_pages=4, max_prefix=700, max_branches=6, max_own=300, Hq=4, Hkv=2)
+    og, lg, O, L = _decode(harness, w, seed)
+    check(og, lg, O, L, "bf16", f"small verify seed {seed}")
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_small_decode_groups(harness, G):
+    w = wl.small_decode(20 + G, n_pages=3, max_prefix=400, max_branches=5, max_own=100, verify=False,
+                        Hq=2 * G, Hkv=2)
+    og, lg, O, L = _decode(harness, w, G, tree=False)
+    check(og, lg, O, L, "bf16", f"decode G={G}")
+
+
+def test_chain_block_without_tree(harness):
+    w = wl.small_decode(9, n_pages=2, max_prefix=300, max_branches=4, max_own=60, verify=True, Hq=4, Hkv=2)
+    og, lg, O, L = _decode(harness, w, 9, tree=False)
+    check(og, lg, O, L, "bf16", "chain block")
+
+
+def test_many_rows_per_page(harness):
+    """More than 128 stacked query rows on one page (several row tiles)."""
+    rng = np.random.default_rng(4)
+    pages = [wl.DecodePage(900, [900] * 12, rng.integers(0, 80, 12).tolist(), [16] * 12,
+                           [wl.draft_tree(rng, max_nodes=16) for _ in range(12)])]
+    for pg in pages:
+        pg.q_len = [len(t) for t in pg.parents]
+    w = wl.DecodeWorkload("rows", pages, 16, 8, 128, 0.5)
+    og, lg, O, L = _decode(harness, w, 4)
+    check(og, lg, O, L, "bf16", "many rows")
+
+
+def test_branch_decode_full(harness):
+    """16 pages, prefix 4809, 8-40 branches, own suffix 0-512: every query."""
+    w = wl.branch_decode(0)
+    og, lg, O, L = _decode(harness, w, 0, tree=False)
+    check(og, lg, O, L, "bf16", "branch decode")
+
+
+def test_page_decode_matches_forward_rows(harness):
+    """Cross-regime: one decode step per content branch of the qwen-shaped
+    page, the cache holding exactly each branch's ancestors, reproduces the
+    forward's rows for the last token of every Y_k."""
+    import torch
+    tree = wl.qwen_page(1)
+    pg = tree.pages[0]
+    q, k, v = wl.tree_qkv(tree, 1)
+    fwd = harness.Forward(tree, q, k, v)
+    o_f, l_f = fwd.run()
+    ident, pos = ta.packed_layout(tree.pages)
+    N = pg.n_regions
+    lay_pos = list(range(pg.prefix_len + sum(pg.layout_len)))
+    own, qpos = [], []
+    for kk in range(N):
+        ys = [pos[(0, ta.Y_KIND, kk, i)] for i in range(pg.content_len[kk])]
+        own.append(ys[:-1])
+        qpos.append(ys[-1])
+    dp = wl.DecodePage(len(lay_pos), [pg.prefix_len + sum(pg.layout_len[: kk + 1]) for kk in range(N)],
+                       [len(o) for o in own], [1] * N, [[-1]] * N)
+    dw = wl.DecodeWorkload("cross", [dp], tree.Hq, tree.Hkv, tree.d, 0.5)
+    vals = wl.DecodeValues([k[lay_pos]], [v[lay_pos]], [k[o] for o in own], [v[o] for o in own],
+                           q[qpos], k[qpos], v[qpos])
+    d = harness.Decode(dw, vals, tree=False)
+    o_d, l_d = d.run()
+    torch.cuda.synchronize()
+    O, L = ta.tree_forward(q, k, v, tree.pages, positions=qpos)
+    check(o_d.float().cpu().numpy(), l_d.cpu().numpy(), O[qpos], L[:, qpos].T, "bf16", "decode vs oracle")
+    check(o_d.float().cpu().numpy(), l_d.cpu().numpy(), o_f.float().cpu().numpy()[qpos],
+          l_f.cpu().numpy()[:, qpos].T, "bf16", "decode vs forward")
+
+
+def test_decode_rejects_bad_batches(harness):
+    import torch
+    w = wl.small_decode(1, n_pages=2, max_prefix=50, max_branches=3, max_own=20, verify=False)
+    d = harness.Decode(w, wl.decode_values(w, 1), tree=False)
+    bad = padoc.Batch(d.page_seq[::-1], [0, 1, len(d.branch_seq)], d.branch_seq,
+                      list(range(len(d.branch_seq) + 1)))
+    with pytest.raises(padoc.PadocError):
+        # branch 0 is not a fork of the sequence now listed first
+        padoc.branch_decode(d.pool, bad, w.Hq, d.q, d.k_new, d.v_new, None, d.o, d.lse, d.ws, d.ws_bytes)
+    with pytest.raises(padoc.PadocError):
+        padoc.branch_decode(d.pool, d.batch, w.Hq, d.q, d.k_new, d.v_new, None, d.o, d.lse, d.ws, 16)
+    torch.cuda.synchronize()

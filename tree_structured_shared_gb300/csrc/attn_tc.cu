@@ -1,0 +1,664 @@
+// Tensor-core attention engine for sm_103a (tcgen05 + TMEM + TMA).
+//
+// One persistent, warp-specialised CTA per SM walks a list of work units.  A
+// unit is 128 query rows (the tokens of one query tile times the query heads
+// of one GQA group, so each K/V tile is read once for the whole group) and the
+// ordered list of 128-key tiles those rows may see:
+//
+//   MODE_FWD     packed tree-varlen forward.  Rows are a tile of one query
+//                segment; key tiles walk that segment's key segments (the
+//                ancestors X, B<=k and the causal own segment).  Tiles of
+//                non-ancestor keys are never listed, so they cost nothing.
+//                (PaDoc, "Training paradigm": Y_k queries attend to the
+//                virtual key/value sequence [X, B<=k, Y_k].)
+//   MODE_PREFIX  cascade prefix pass of branch decode.  Rows are the query
+//                rows of every branch of one page; key tiles are one chunk of
+//                the page's shared prefix blocks, read from HBM once for all
+//                branches (HPD-Parsing: forked branches share the prefix KV
+//                with zero copy).  Writes normalised partial O and LSE.
+//
+// Roles (192 threads):
+//   warps 0-3  softmax: thread r owns TMEM lane r = query row r.  Reads S from
+//              TMEM, masks, keeps the running max / sum, writes P (bf16) to
+//              shared memory, rescales O in TMEM when the max grows by more
+//              than 2^8, and runs the epilogue.
+//   warp 4     producer: TMA loads of Q (or a gather for decode rows), K, V.
+//   warp 5     MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
+//              tile, O += P V into a TMEM accumulator.
+//
+// TMEM: columns [0,128) and [128,256) hold S, [256,384) hold O (f32).
+// Shared memory (1024-byte aligned, 128-byte swizzle, two 64-column halves):
+//   Q 32 KB | K 2 x 32 KB | V 2 x 32 KB | P 2 x 32 KB | barriers.
+// Every wait is bounded; a unit that times out raises the CTA abort flag, the
+// device error word, and all roles leave their loops.
+#include <cuda_bf16.h>
+
+#include "../../include/padoc.h"
+#include "padoc_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace padoc {
+
+__device__ unsigned int g_tc_err;
+
+namespace {
+
+using namespace ptx;
+
+enum { MODE_FWD = 0, MODE_PREFIX = 1 };
+
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr int kHalf = 16384;  // bytes of one 64-column half of a 128-row tile
+constexpr int SM_Q = 0;
+constexpr int SM_K = SM_Q + 2 * kHalf;
+constexpr int SM_V = SM_K + kStages * 2 * kHalf;
+constexpr int SM_P = SM_V + kStages * 2 * kHalf;
+constexpr int SM_BAR = SM_P + 2 * 2 * kHalf;
+constexpr int SM_TOTAL = SM_BAR + 256;
+constexpr int kSmemBytes = SM_TOTAL + 1024;
+
+// barrier slots
+enum {
+  B_Q_FULL = 0,
+  B_Q_EMPTY = 1,
+  B_K_FULL = 2,   // +stage
+  B_K_EMPTY = 4,  // +stage
+  B_V_FULL = 6,
+  B_V_EMPTY = 8,
+  B_S_FULL = 10,  // +buffer
+  B_S_FREE = 12,
+  B_P_FULL = 14,
+  B_P_EMPTY = 16,
+  B_O_DONE = 18,
+  B_O_FREE = 19,
+  N_BARS = 20
+};
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+struct Params {
+  int mode;
+  int n_units;
+  int32_t Hq, Hkv, group;
+  float sl2;  // scale * log2(e)
+  // forward
+  FwdPlan plan;
+  int64_t T;
+  __nv_bfloat16* o;
+  float* lse;
+  // prefix pass
+  const DecPage* pages;
+  const DecItem* items;
+  const int32_t* q_plen;
+  const int32_t* table;
+  int32_t max_bps;
+  const __nv_bfloat16* q;
+  float* part_o;
+  float* part_lse;
+};
+
+// The work unit as seen by every role (computed identically by each).
+struct Unit {
+  int32_t g;         // kv head
+  // forward
+  int32_t tile_start, q_end, kv_first, kv_count, tile_last;
+  // prefix
+  int32_t page, tile, rows, row_base, k_begin, k_end, seq, q_first;
+};
+
+__device__ __forceinline__ Unit load_unit(const Params& p, int u) {
+  Unit w;
+  w.g = u % p.Hkv;
+  const int item = u / p.Hkv;
+  if (p.mode == MODE_FWD) {
+    const FwdItem it = p.plan.items[item];
+    const QSeg qs = p.plan.qsegs[it.qseg];
+    w.tile_start = it.tile_start;
+    w.q_end = qs.q_start + qs.q_len;
+    w.kv_first = qs.kv_first;
+    w.kv_count = qs.kv_count;
+    w.tile_last = min(it.tile_start + p.plan.tile_tokens, w.q_end) - 1;
+  } else {
+    const DecItem it = p.items[item];
+    const DecPage pg = p.pages[it.page];
+    w.page = it.page;
+    w.tile = it.tile;
+    w.rows = it.rows;
+    w.row_base = it.row_base;
+    w.k_begin = it.chunk * pg.chunk_tokens;
+    w.k_end = min(pg.P, w.k_begin + pg.chunk_tokens);
+    w.seq = pg.seq;
+    w.q_first = pg.q_first;
+  }
+  return w;
+}
+
+// Key tiles of a unit are enumerated in one fixed order by every role.
+struct TileIter {
+  int32_t s, s_end, ks, end, causal;
+};
+
+__device__ __forceinline__ bool seg_setup(const Params& p, const Unit& w, TileIter& t) {
+  while (t.s < t.s_end) {
+    const KVSeg kv = p.plan.kvsegs[t.s];
+    int32_t end = kv.start + kv.len;
+    if (kv.causal) end = min(end, w.tile_last + 1);
+    if (end > kv.start) {
+      t.ks = kv.start;
+      t.end = end;
+      t.causal = kv.causal;
+      return true;
+    }
+    ++t.s;
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool tiles_begin(const Params& p, const Unit& w, TileIter& t) {
+  if (p.mode == MODE_FWD) {
+    t.s = w.kv_first;
+    t.s_end = w.kv_first + w.kv_count;
+    return seg_setup(p, w, t);
+  }
+  t.s = 0;
+  t.s_end = 1;
+  t.ks = w.k_begin;
+  t.end = w.k_end;
+  t.causal = 0;
+  return t.ks < t.end;
+}
+
+__device__ __forceinline__ bool tiles_next(const Params& p, const Unit& w, TileIter& t) {
+  t.ks += kTileKeys;
+  if (t.ks < t.end) return true;
+  if (p.mode == MODE_FWD) {
+    ++t.s;
+    return seg_setup(p, w, t);
+  }
+  return false;
+}
+
+__device__ __forceinline__ int count_tiles(const Params& p, const Unit& w) {
+  int n = 0;
+  TileIter t;
+  for (bool ok = tiles_begin(p, w, t); ok; ok = tiles_next(p, w, t)) ++n;
+  return n;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort, unsigned site) {
+  *abort = 1;
+  atomicOr(&g_tc_err, site);
+}
+
+// Byte offset of 16-byte chunk c (0..15) of row r in a two-half, 128-row,
+// 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (c >> 3) * kHalf + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_BAR + N_BARS * 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + SM_BAR + N_BARS * 8 + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < N_BARS; ++i) {
+      uint32_t cnt = 1;
+      if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_FREE) cnt = 4;
+      mbar_init(bar(i), cnt);
+    }
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (MODE == MODE_PREFIX) {
+    // stale bytes in a partly filled K/V tile are masked, but must be finite
+    uint4 z = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < (SM_P - SM_K) / 16; i += kThreads)
+      reinterpret_cast<uint4*>(smem + SM_K)[i] = z;
+    fence_proxy_async_smem();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int G = p.group;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && MODE == MODE_FWD) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    uint32_t kv_it = 0, item_it = 0;
+    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+      const Unit w = load_unit(p, u);
+      if (count_tiles(p, w) == 0) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (item_it & 1) ^ 1, abort))) {
+        if (lane == 0) raise_abort(abort, 0x1);
+        break;
+      }
+      if (MODE == MODE_FWD) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * kHalf);
+          const int tt = p.plan.tile_tokens;
+          for (int hh = 0; hh < G; ++hh)
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(sbase + SM_Q + h * kHalf + hh * tt * 128, &tm_q, bar(B_Q_FULL), h * 64, w.g * G + hh,
+                          w.tile_start);
+        }
+      } else {
+        // gather the page's query rows: row R = query (R / G), head g*G + R % G
+        const uint4* q4 = reinterpret_cast<const uint4*>(p.q);
+        for (int x = lane; x < kTileRows * 16; x += 32) {
+          const int r = x >> 4, c = x & 15;
+          uint4 val = make_uint4(0, 0, 0, 0);
+          if (r < w.rows) {
+            const int R = w.tile * kTileRows + r;
+            const int64_t qi = w.q_first + R / G;
+            const int head = w.g * G + R % G;
+            val = q4[(qi * p.Hq + head) * 16 + c];
+          }
+          *reinterpret_cast<uint4*>(smem + SM_Q + sw128_off(r, c)) = val;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_Q_FULL));
+      }
+      TileIter t;
+      bool failed = false;
+      for (bool ok = tiles_begin(p, w, t); ok; ok = tiles_next(p, w, t), ++kv_it) {
+        const int st = kv_it % kStages;
+        const uint32_t ph = ((kv_it / kStages) & 1) ^ 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_K_EMPTY + st), ph, abort))) { failed = true; break; }
+        if (MODE == MODE_FWD) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_K_FULL + st), 2 * kHalf);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(sbase + SM_K + st * 2 * kHalf + h * kHalf, &tm_k, bar(B_K_FULL + st), h * 64, w.g, t.ks);
+          }
+        } else {
+          const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
+          int32_t blk = 0;
+          if (lane < nblk) blk = p.table[static_cast<int64_t>(w.seq) * p.max_bps + (t.ks >> 4) + lane];
+          if (lane == 0) mbar_arrive_expect_tx(bar(B_K_FULL + st), nblk * 2 * 2048);
+          __syncwarp();
+          if (lane < nblk) {
+            const int32_t row = (blk * p.Hkv + w.g) * 16;
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(sbase + SM_K + st * 2 * kHalf + h * kHalf + lane * 2048, &tm_k, bar(B_K_FULL + st),
+                          h * 64, row);
+          }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_V_EMPTY + st), ph, abort))) { failed = true; break; }
+        if (MODE == MODE_FWD) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_V_FULL + st), 2 * kHalf);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(sbase + SM_V + st * 2 * kHalf + h * kHalf, &tm_v, bar(B_V_FULL + st), h * 64, w.g, t.ks);
+          }
+        } else {
+          const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
+          int32_t blk = 0;
+          if (lane < nblk) blk = p.table[static_cast<int64_t>(w.seq) * p.max_bps + (t.ks >> 4) + lane];
+          if (lane == 0) mbar_arrive_expect_tx(bar(B_V_FULL + st), nblk * 2 * 2048);
+          __syncwarp();
+          if (lane < nblk) {
+            const int32_t row = (blk * p.Hkv + w.g) * 16;
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(sbase + SM_V + st * 2 * kHalf + h * kHalf + lane * 2048, &tm_v, bar(B_V_FULL + st),
+                          h * 64, row);
+          }
+        }
+      }
+      if (failed) {
+        if (lane == 0) raise_abort(abort, 0x2);
+        break;
+      }
+      ++item_it;
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t t_o = tmem + 256;
+      uint32_t k_it = 0, v_it = 0, s_it = 0, p_it = 0, item_it = 0;
+      bool failed = false;
+      auto issue_s = [&]() -> bool {
+        const int st = k_it % kStages;
+        const int sb = s_it & 1;
+        if (!mbar_wait(bar(B_K_FULL + st), (k_it / kStages) & 1, abort)) return false;
+        if (!mbar_wait(bar(B_S_FREE + sb), ((s_it >> 1) & 1) ^ 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t qa = sbase + SM_Q;
+        const uint32_t ka = sbase + SM_K + st * 2 * kHalf;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          mma_bf16_ss(tmem + sb * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), id_qk,
+                      kk > 0);
+        }
+        mma_commit(bar(B_S_FULL + sb));
+        mma_commit(bar(B_K_EMPTY + st));
+        ++k_it;
+        ++s_it;
+        return true;
+      };
+      for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+        const Unit w = load_unit(p, u);
+        const int n = count_tiles(p, w);
+        if (n == 0) continue;
+        if (!mbar_wait(bar(B_Q_FULL), item_it & 1, abort)) { failed = true; break; }
+        if (!issue_s()) { failed = true; break; }
+        for (int j = 0; j < n; ++j) {
+          if (j + 1 < n) {
+            if (!issue_s()) { failed = true; break; }
+          } else {
+            mma_commit(bar(B_Q_EMPTY));
+          }
+          const int st = v_it % kStages;
+          const int pb = p_it & 1;
+          if (j == 0 && !mbar_wait(bar(B_O_FREE), (item_it & 1) ^ 1, abort)) { failed = true; break; }
+          if (!mbar_wait(bar(B_P_FULL + pb), (p_it >> 1) & 1, abort)) { failed = true; break; }
+          if (!mbar_wait(bar(B_V_FULL + st), (v_it / kStages) & 1, abort)) { failed = true; break; }
+          tc_fence_after();
+          const uint32_t pa = sbase + SM_P + pb * 2 * kHalf;
+          const uint32_t va = sbase + SM_V + st * 2 * kHalf;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
+            mma_bf16_ss(t_o, sdesc_sw128(pa + aoff, 16, 1024), sdesc_sw128(va + kk * 2048, kHalf, 1024), id_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(B_P_EMPTY + pb));
+          mma_commit(bar(B_V_EMPTY + st));
+          mma_commit(bar(B_O_DONE));
+          ++v_it;
+          ++p_it;
+        }
+        ++item_it;
+      }
+      if (failed) raise_abort(abort, 0x4);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-3)
+    const int r = threadIdx.x;  // query row == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t s_it = 0, p_it = 0, pv_base = 0;
+    bool failed = false;
+    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+      const Unit w = load_unit(p, u);
+      const int n = count_tiles(p, w);
+      if (n == 0) continue;
+      // this thread's row
+      bool valid;
+      int32_t head, limit;  // limit: keys at positions >= limit are hidden (prefix) / causal bound (fwd)
+      int64_t qpos = 0;
+      if (MODE == MODE_FWD) {
+        const int tt = p.plan.tile_tokens;
+        const int hh = r / tt;
+        qpos = w.tile_start + (r % tt);
+        valid = qpos < w.q_end;
+        head = w.g * G + hh;
+        limit = static_cast<int32_t>(qpos) + 1;
+      } else {
+        valid = r < w.rows;
+        const int R = w.tile * kTileRows + r;
+        head = w.g * G + R % G;
+        qpos = w.q_first + R / G;
+        limit = valid ? p.q_plen[qpos] : 0;
+      }
+      float m_run = -INFINITY, l_run = 0.f;
+      TileIter t;
+      int j = 0;
+      for (bool ok = tiles_begin(p, w, t); ok; ok = tiles_next(p, w, t), ++j) {
+        const int sb = s_it & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + sb), (s_it >> 1) & 1, abort))) { failed = true; break; }
+        tc_fence_after();
+        float s[128];
+        {
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tmem + lane_base + sb * 128 + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_S_FREE + sb));
+        ++s_it;
+        // mask keys this row may not see
+        const int32_t klen = min(kTileKeys, t.end - t.ks);
+        int32_t vis = klen;  // keys [0, vis) of the tile are visible
+        if (MODE == MODE_FWD) {
+          if (t.causal) vis = min(vis, limit - t.ks);
+        } else {
+          vis = min(vis, limit - t.ks);
+        }
+        if (vis < kTileKeys) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= vis) s[c] = -INFINITY;
+        }
+        float tmax = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) tmax = fmaxf(tmax, s[c]);
+        const float mt = tmax * p.sl2;
+        const bool grow = mt > m_run + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow) && j > 0) {
+          // O holds sums with the old max: rescale it before the next P V lands
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (pv_base + j - 1) & 1, abort))) { failed = true; break; }
+          tc_fence_after();
+          const float alpha = grow ? fast_exp2(m_run - mt) : 1.f;
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tmem + 256 + lane_base + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tmem + 256 + lane_base + c * 32, v);
+          }
+          tmem_wait_st();
+        }
+        if (grow) {
+          l_run *= fast_exp2(m_run - mt);
+          m_run = mt;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          s[c] = fast_exp2(fmaf(s[c], p.sl2, -m_use));
+          lsum += s[c];
+        }
+        l_run += lsum;
+        const int pb = p_it & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_P_EMPTY + pb), ((p_it >> 1) & 1) ^ 1, abort))) { failed = true; break; }
+        const uint32_t pa = sbase + SM_P + pb * 2 * kHalf;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_shared_v4(pa + sw128_off(r, c), pack_bf16x2(s[8 * c + 0], s[8 * c + 1]),
+                       pack_bf16x2(s[8 * c + 2], s[8 * c + 3]), pack_bf16x2(s[8 * c + 4], s[8 * c + 5]),
+                       pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_P_FULL + pb));
+        ++p_it;
+      }
+      if (failed) break;
+      // epilogue: O / l and LSE
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (pv_base + n - 1) & 1, abort))) { failed = true; break; }
+      tc_fence_after();
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + 256 + lane_base + c * 32, v);
+        tmem_wait_ld();
+        if (valid) {
+          if (MODE == MODE_FWD) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + (qpos * p.Hq + head) * kHeadDim + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * inv_l, __uint_as_float(v[8 * i + 1]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv_l, __uint_as_float(v[8 * i + 3]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv_l, __uint_as_float(v[8 * i + 5]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv_l, __uint_as_float(v[8 * i + 7]) * inv_l));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(
+                p.part_o + (static_cast<int64_t>(w.row_base) + static_cast<int64_t>(w.g) * w.rows + r) * kHeadDim + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i + 0]) * inv_l, __uint_as_float(v[4 * i + 1]) * inv_l,
+                                   __uint_as_float(v[4 * i + 2]) * inv_l, __uint_as_float(v[4 * i + 3]) * inv_l);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_O_FREE));
+      if (valid) {
+        if (MODE == MODE_FWD)
+          p.lse[static_cast<int64_t>(head) * p.T + qpos] = lse_v;
+        else
+          p.part_lse[static_cast<int64_t>(w.row_base) + static_cast<int64_t>(w.g) * w.rows + r] = lse_v;
+      }
+      pv_base += n;
+    }
+    if (failed && lane == 0) raise_abort(abort, 0x8);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+int make_map(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+             const cuuint64_t* strides, const cuuint32_t* box, std::string* err) {
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed with code " + std::to_string(static_cast<int>(r));
+    return PADOC_ERR_CUDA;
+  }
+  return PADOC_OK;
+}
+
+template <int MODE>
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm, cudaStream_t s,
+           std::string* err) {
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[MODE]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) {
+      *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+      return PADOC_ERR_CUDA;
+    }
+    attr_set[MODE] = true;
+  }
+  const int grid = std::min(prm.n_units, num_sms());
+  attn_tc_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string("attention kernel launch: ") + cudaGetErrorString(e);
+    return PADOC_ERR_CUDA;
+  }
+  return PADOC_OK;
+}
+
+}  // namespace
+
+int launch_fwd_bf16(const FwdArgs& a, cudaStream_t s, std::string* err) {
+  if (a.plan.n_items == 0) return PADOC_OK;
+  EncodeTiledFn enc = get_encode_fn(err);
+  if (!enc) return PADOC_ERR_CUDA;
+  CUtensorMap mq, mk, mv;
+  const cuuint64_t dq[3] = {128, static_cast<cuuint64_t>(a.Hq), static_cast<cuuint64_t>(a.T)};
+  const cuuint64_t sq[2] = {256, static_cast<cuuint64_t>(a.Hq) * 256};
+  const cuuint32_t bq[3] = {64, 1, static_cast<cuuint32_t>(a.plan.tile_tokens)};
+  const cuuint64_t dk[3] = {128, static_cast<cuuint64_t>(a.Hkv), static_cast<cuuint64_t>(a.T)};
+  const cuuint64_t sk[2] = {256, static_cast<cuuint64_t>(a.Hkv) * 256};
+  const cuuint32_t bk[3] = {64, 1, 128};
+  int rc = make_map(enc, &mq, a.q, 3, dq, sq, bq, err);
+  if (!rc) rc = make_map(enc, &mk, a.k, 3, dk, sk, bk, err);
+  if (!rc) rc = make_map(enc, &mv, a.v, 3, dk, sk, bk, err);
+  if (rc) return rc;
+  Params p{};
+  p.mode = MODE_FWD;
+  p.n_units = a.plan.n_items * a.Hkv;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.group = a.plan.group;
+  p.sl2 = a.scale * kLog2e;
+  p.plan = a.plan;
+  p.T = a.T;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  return launch<MODE_FWD>(mq, mk, mv, p, s, err);
+}
+
+int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err) {
+  if (a.n_items == 0) return PADOC_OK;
+  EncodeTiledFn enc = get_encode_fn(err);
+  if (!enc) return PADOC_ERR_CUDA;
+  CUtensorMap mk, mv;
+  const cuuint64_t dk[2] = {128, static_cast<cuuint64_t>(a.num_blocks) * a.Hkv * 16};
+  const cuuint64_t sk[1] = {256};
+  const cuuint32_t bk[2] = {64, 16};
+  int rc = make_map(enc, &mk, a.k_pool, 2, dk, sk, bk, err);
+  if (!rc) rc = make_map(enc, &mv, a.v_pool, 2, dk, sk, bk, err);
+  if (rc) return rc;
+  Params p{};
+  p.mode = MODE_PREFIX;
+  p.n_units = a.n_items * a.Hkv;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.group = a.group;
+  p.sl2 = a.scale * kLog2e;
+  p.pages = a.pages;
+  p.items = a.items;
+  p.q_plen = a.q_plen;
+  p.table = a.table;
+  p.max_bps = a.max_bps;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.part_o = a.part_o;
+  p.part_lse = a.part_lse;
+  return launch<MODE_PREFIX>(mk, mk, mv, p, s, err);
+}
+
+int read_and_clear_tc_error(cudaStream_t s, unsigned* word) {
+  unsigned zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_tc_err, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_tc_err, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? PADOC_OK : PADOC_ERR_CUDA;
+}
+
+}  // namespace padoc

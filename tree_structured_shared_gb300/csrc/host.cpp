@@ -1,0 +1,941 @@
+// libpadoc host side: error reporting, the tree-descriptor builder, the
+// refcounted paged KV pool, decode planning and the C ABI entry points.
+#include "../../include/padoc.h"
+#include "padoc_internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <memory>
+#include <new>
+#include <numeric>
+#include <string>
+#include <vector>
+
+using namespace padoc;
+
+// ============================================================== errors
+
+static thread_local std::string g_last_error;
+
+static int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+static int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PADOC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define PADOC_TRY(...)                                                      \
+  try {                                                                     \
+    __VA_ARGS__;                                                            \
+  } catch (const std::bad_alloc&) {                                         \
+    return fail(PADOC_ERR_OOM, "host allocation failed");                   \
+  } catch (...) {                                                           \
+    return fail(PADOC_ERR_INVALID, "unexpected host exception");            \
+  }
+
+extern "C" const char* padoc_last_error(void) { return g_last_error.c_str(); }
+extern "C" int padoc_version(void) { return 100; }
+
+namespace padoc {
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n > 0 ? n : 148;
+}
+
+EncodeTiledFn get_encode_fn(std::string* err) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!fn && err) *err = "cuTensorMapEncodeTiled is not available from the driver";
+  return fn;
+}
+
+}  // namespace padoc
+
+// ============================================================== tree descriptor
+
+struct Run {
+  int64_t start, len;
+  bool causal;
+};
+
+struct DevPlan {
+  int device = -1;
+  int group = 0;
+  int tile_tokens = 0;
+  QSeg* qsegs = nullptr;
+  KVSeg* kvsegs = nullptr;
+  FwdItem* items = nullptr;
+  int32_t n_items = 0;
+};
+
+struct padoc_tree_desc {
+  int64_t T = 0;
+  int64_t pairs = 0;
+  std::vector<QSeg> qsegs;
+  std::vector<KVSeg> kvsegs;
+  std::vector<DevPlan> dev;
+  ~padoc_tree_desc() {
+    for (auto& d : dev) {
+      int cur = -1;
+      cudaGetDevice(&cur);
+      if (d.device >= 0) cudaSetDevice(d.device);
+      cudaFree(d.qsegs);
+      cudaFree(d.kvsegs);
+      cudaFree(d.items);
+      if (cur >= 0) cudaSetDevice(cur);
+    }
+  }
+};
+
+namespace {
+
+// Query region with its key runs, in packing order.
+struct Region {
+  int64_t q_start, q_len;
+  std::vector<Run> runs;  // ordered; the last is causal and contains the queries
+};
+
+// Merges position-adjacent runs; a full run directly before the causal run
+// joins it (all of its keys precede every query of the region).
+std::vector<Run> merge_runs(const std::vector<Run>& in) {
+  std::vector<Run> out;
+  for (const Run& r : in) {
+    if (r.len <= 0 && !r.causal) continue;
+    if (!out.empty() && out.back().start + out.back().len == r.start && !out.back().causal) {
+      out.back().len += r.len;
+      out.back().causal = r.causal;
+    } else {
+      out.push_back(r);
+    }
+  }
+  return out;
+}
+
+// Region B may extend region A (same key runs, causal run grown to cover B).
+bool extends(const Region& a, const Region& b) {
+  if (a.q_start + a.q_len != b.q_start || a.runs.size() != b.runs.size()) return false;
+  for (size_t i = 0; i + 1 < a.runs.size(); ++i)
+    if (a.runs[i].start != b.runs[i].start || a.runs[i].len != b.runs[i].len ||
+        a.runs[i].causal != b.runs[i].causal)
+      return false;
+  const Run& ra = a.runs.back();
+  const Run& rb = b.runs.back();
+  return ra.causal && rb.causal && ra.start == rb.start && ra.start + ra.len == a.q_start + a.q_len &&
+         rb.start + rb.len == b.q_start + b.q_len;
+}
+
+}  // namespace
+
+extern "C" int padoc_tree_desc_build(const padoc_tree_spec* spec, padoc_tree_desc** out) {
+  if (!spec || !out) return fail(PADOC_ERR_INVALID, "tree_desc_build: null argument");
+  *out = nullptr;
+  if (spec->n_pages < 0) return fail(PADOC_ERR_INVALID, "tree_desc_build: n_pages < 0");
+  if (spec->order != PADOC_PACK_CANONICAL && spec->order != PADOC_PACK_DOCUMENT)
+    return fail(PADOC_ERR_INVALID, "tree_desc_build: unknown packing order %d", spec->order);
+  if (spec->n_pages > 0 && (!spec->prefix_len || !spec->n_regions))
+    return fail(PADOC_ERR_INVALID, "tree_desc_build: null page arrays");
+  padoc_tree_desc* d = nullptr;
+  PADOC_TRY({
+    std::unique_ptr<padoc_tree_desc> desc(new padoc_tree_desc());
+    int64_t off = 0;
+    int64_t ridx = 0;
+    std::vector<Region> regions;
+    for (int32_t p = 0; p < spec->n_pages; ++p) {
+      const int64_t P = spec->prefix_len[p];
+      const int32_t N = spec->n_regions[p];
+      if (P < 0 || N < 0) return fail(PADOC_ERR_INVALID, "tree_desc_build: page %d negative size", p);
+      if (N > 0 && (!spec->layout_len || !spec->content_len))
+        return fail(PADOC_ERR_INVALID, "tree_desc_build: null region arrays");
+      std::vector<int64_t> lay(N), con(N), bpos(N), ypos(N);
+      int64_t total = P;
+      for (int32_t k = 0; k < N; ++k) {
+        lay[k] = spec->layout_len[ridx + k];
+        con[k] = spec->content_len[ridx + k];
+        if (lay[k] < 0 || con[k] < 0)
+          return fail(PADOC_ERR_INVALID, "tree_desc_build: page %d region %d negative length", p, k);
+        total += lay[k] + con[k];
+      }
+      ridx += N;
+      if (off + total >= (int64_t(1) << 31))
+        return fail(PADOC_ERR_INVALID, "tree_desc_build: more than 2^31 - 1 tokens");
+      // positions
+      int64_t cur = off + P;
+      if (spec->order == PADOC_PACK_CANONICAL) {
+        for (int32_t k = 0; k < N; ++k) { bpos[k] = cur; cur += lay[k]; }
+        for (int32_t k = 0; k < N; ++k) { ypos[k] = cur; cur += con[k]; }
+      } else {
+        for (int32_t k = 0; k < N; ++k) {
+          bpos[k] = cur; cur += lay[k];
+          ypos[k] = cur; cur += con[k];
+        }
+      }
+      // regions in packing order: X, then B/Y by position
+      std::vector<Region> page_regions;
+      if (P > 0) page_regions.push_back({off, P, {{off, P, true}}});
+      for (int32_t k = 0; k < N; ++k) {
+        if (lay[k] > 0) {  // Anc(B_k) = {X, B<k} plus B_k up to the query
+          std::vector<Run> r{{off, P, false}};
+          for (int32_t i = 0; i < k; ++i) r.push_back({bpos[i], lay[i], false});
+          r.push_back({bpos[k], lay[k], true});
+          page_regions.push_back({bpos[k], lay[k], merge_runs(r)});
+        }
+        if (con[k] > 0) {  // Anc(Y_k) = {X, B<=k} plus Y_k up to the query
+          std::vector<Run> r{{off, P, false}};
+          for (int32_t i = 0; i <= k; ++i) r.push_back({bpos[i], lay[i], false});
+          r.push_back({ypos[k], con[k], true});
+          page_regions.push_back({ypos[k], con[k], merge_runs(r)});
+        }
+      }
+      std::sort(page_regions.begin(), page_regions.end(),
+                [](const Region& a, const Region& b) { return a.q_start < b.q_start; });
+      for (Region& r : page_regions) {
+        if (!regions.empty() && extends(regions.back(), r)) {
+          Region& a = regions.back();
+          a.q_len += r.q_len;
+          a.runs.back().len = r.runs.back().len;
+        } else {
+          regions.push_back(std::move(r));
+        }
+      }
+      off += total;
+    }
+    desc->T = off;
+    int64_t pairs = 0;
+    for (const Region& r : regions) {
+      QSeg q;
+      q.q_start = static_cast<int32_t>(r.q_start);
+      q.q_len = static_cast<int32_t>(r.q_len);
+      q.kv_first = static_cast<int32_t>(desc->kvsegs.size());
+      q.kv_count = static_cast<int32_t>(r.runs.size());
+      desc->qsegs.push_back(q);
+      for (const Run& run : r.runs) {
+        desc->kvsegs.push_back({static_cast<int32_t>(run.start), static_cast<int32_t>(run.len),
+                                run.causal ? 1 : 0, 0});
+        if (run.causal) {
+          const int64_t a = r.q_start - run.start + 1;  // keys seen by the first query
+          pairs += r.q_len * a + r.q_len * (r.q_len - 1) / 2;
+        } else {
+          pairs += r.q_len * run.len;
+        }
+      }
+    }
+    desc->pairs = pairs;
+    d = desc.release();
+  });
+  *out = d;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_tree_desc_free(padoc_tree_desc* desc) {
+  delete desc;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_tree_desc_info(const padoc_tree_desc* desc, int64_t* n_tokens, int64_t* n_qsegs,
+                                    int64_t* n_kvsegs, int64_t* ancestor_pairs) {
+  if (!desc) return fail(PADOC_ERR_INVALID, "tree_desc_info: null descriptor");
+  if (n_tokens) *n_tokens = desc->T;
+  if (n_qsegs) *n_qsegs = static_cast<int64_t>(desc->qsegs.size());
+  if (n_kvsegs) *n_kvsegs = static_cast<int64_t>(desc->kvsegs.size());
+  if (ancestor_pairs) *ancestor_pairs = desc->pairs;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_tree_desc_segments(const padoc_tree_desc* desc, int32_t* qseg, int32_t* kvseg) {
+  if (!desc) return fail(PADOC_ERR_INVALID, "tree_desc_segments: null descriptor");
+  if (qseg)
+    for (size_t i = 0; i < desc->qsegs.size(); ++i) {
+      qseg[4 * i + 0] = desc->qsegs[i].q_start;
+      qseg[4 * i + 1] = desc->qsegs[i].q_len;
+      qseg[4 * i + 2] = desc->qsegs[i].kv_first;
+      qseg[4 * i + 3] = desc->qsegs[i].kv_count;
+    }
+  if (kvseg)
+    for (size_t i = 0; i < desc->kvsegs.size(); ++i) {
+      kvseg[3 * i + 0] = desc->kvsegs[i].start;
+      kvseg[3 * i + 1] = desc->kvsegs[i].len;
+      kvseg[3 * i + 2] = desc->kvsegs[i].causal;
+    }
+  return PADOC_OK;
+}
+
+// Query tiles of tile_tokens tokens, longest key walk first (LPT order).
+static std::vector<FwdItem> build_items(const padoc_tree_desc* desc, int tile_tokens) {
+  struct Cost {
+    int64_t cost;
+    FwdItem it;
+  };
+  std::vector<Cost> v;
+  for (size_t s = 0; s < desc->qsegs.size(); ++s) {
+    const QSeg& q = desc->qsegs[s];
+    for (int32_t t0 = q.q_start; t0 < q.q_start + q.q_len; t0 += tile_tokens) {
+      const int32_t t1 = std::min(t0 + tile_tokens, q.q_start + q.q_len);
+      int64_t c = 0;
+      for (int32_t j = 0; j < q.kv_count; ++j) {
+        const KVSeg& kv = desc->kvsegs[q.kv_first + j];
+        int64_t len = kv.len;
+        if (kv.causal) len = std::min<int64_t>(kv.len, t1 - kv.start);
+        c += (len + kTileKeys - 1) / kTileKeys;
+      }
+      v.push_back({c, {static_cast<int32_t>(s), t0}});
+    }
+  }
+  std::stable_sort(v.begin(), v.end(), [](const Cost& a, const Cost& b) { return a.cost > b.cost; });
+  std::vector<FwdItem> out(v.size());
+  for (size_t i = 0; i < v.size(); ++i) out[i] = v[i].it;
+  return out;
+}
+
+static int upload_desc(padoc_tree_desc* desc, int group, DevPlan** plan_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  for (auto& p : desc->dev)
+    if (p.device == dev && p.group == group) {
+      *plan_out = &p;
+      return PADOC_OK;
+    }
+  DevPlan p;
+  p.device = dev;
+  p.group = group;
+  p.tile_tokens = kTileRows / group;
+  std::vector<FwdItem> items;
+  PADOC_TRY(items = build_items(desc, p.tile_tokens));
+  p.n_items = static_cast<int32_t>(items.size());
+  auto alloc_copy = [](void** dst, const void* src, size_t bytes) -> cudaError_t {
+    if (bytes == 0) bytes = 16;
+    cudaError_t e2 = cudaMalloc(dst, bytes);
+    if (e2 != cudaSuccess) return e2;
+    if (src) return cudaMemcpy(*dst, src, bytes, cudaMemcpyHostToDevice);
+    return cudaSuccess;
+  };
+  e = alloc_copy(reinterpret_cast<void**>(&p.qsegs), desc->qsegs.data(), desc->qsegs.size() * sizeof(QSeg));
+  if (e == cudaSuccess)
+    e = alloc_copy(reinterpret_cast<void**>(&p.kvsegs), desc->kvsegs.data(), desc->kvsegs.size() * sizeof(KVSeg));
+  if (e == cudaSuccess)
+    e = alloc_copy(reinterpret_cast<void**>(&p.items), items.data(), items.size() * sizeof(FwdItem));
+  if (e != cudaSuccess) {
+    cudaFree(p.qsegs);
+    cudaFree(p.kvsegs);
+    cudaFree(p.items);
+    return cuda_fail(e, "tree descriptor upload");
+  }
+  desc->dev.push_back(p);
+  *plan_out = &desc->dev.back();
+  return PADOC_OK;
+}
+
+static bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+extern "C" int padoc_tree_desc_upload(padoc_tree_desc* desc, int32_t group) {
+  if (!desc) return fail(PADOC_ERR_INVALID, "tree_desc_upload: null descriptor");
+  if (!valid_group(group)) return fail(PADOC_ERR_INVALID, "tree_desc_upload: group %d not in {1,2,4,8,16}", group);
+  DevPlan* p = nullptr;
+  return upload_desc(desc, group, &p);
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" int padoc_tree_attn_varlen(padoc_tree_desc* desc, const void* q, const void* k, const void* v,
+                                      void* o, float* lse, int32_t dtype, int32_t Hq, int32_t Hkv,
+                                      int32_t d, float scale, padoc_stream_t stream) {
+  if (!desc) return fail(PADOC_ERR_INVALID, "tree_attn_varlen: null descriptor");
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return fail(PADOC_ERR_INVALID, "tree_attn_varlen: Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  const int group = Hq / Hkv;
+  if (!valid_group(group)) return fail(PADOC_ERR_UNSUPPORTED, "tree_attn_varlen: Hq/Hkv=%d not in {1,2,4,8,16}", group);
+  if (dtype == PADOC_BF16) {
+    if (d != kHeadDim) return fail(PADOC_ERR_UNSUPPORTED, "tree_attn_varlen: bf16 path needs d=128 (got %d)", d);
+  } else if (dtype == PADOC_F32) {
+    if (d != 64 && d != 128) return fail(PADOC_ERR_UNSUPPORTED, "tree_attn_varlen: f32 path needs d in {64,128}");
+  } else {
+    return fail(PADOC_ERR_INVALID, "tree_attn_varlen: unknown dtype %d", dtype);
+  }
+  if (desc->T == 0) return PADOC_OK;
+  if (!q || !k || !v || !o || !lse) return fail(PADOC_ERR_INVALID, "tree_attn_varlen: null tensor");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(PADOC_ERR_INVALID, "tree_attn_varlen: tensors must be 16-byte aligned");
+  DevPlan* plan = nullptr;
+  int rc = upload_desc(desc, group, &plan);
+  if (rc) return rc;
+  FwdArgs a;
+  a.plan = {plan->qsegs, plan->kvsegs, plan->items, plan->n_items, group, plan->tile_tokens};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.T = desc->T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
+  std::string err;
+  rc = dtype == PADOC_BF16 ? launch_fwd_bf16(a, reinterpret_cast<cudaStream_t>(stream), &err)
+                           : launch_fwd_f32(a, reinterpret_cast<cudaStream_t>(stream), &err);
+  if (rc) return fail(rc, "tree_attn_varlen: %s", err.c_str());
+  return PADOC_OK;
+}
+
+// ============================================================== KV pool
+
+struct Seq {
+  bool live = false;
+  int32_t len = 0;       // tokens
+  int32_t fork_len = 0;  // leading tokens shared from the fork parent
+  int32_t n_shared = 0;  // leading blocks shared from the fork parent
+  std::vector<int32_t> blocks;
+};
+
+struct padoc_kv_pool {
+  void* k = nullptr;
+  void* v = nullptr;
+  int32_t nb = 0, bs = 16, Hkv = 0, d = 0, dtype = 0, max_seqs = 0, max_bps = 0;
+  std::vector<int32_t> refcnt;
+  std::vector<int32_t> free_blocks;  // stack
+  std::vector<Seq> seqs;
+  std::vector<int32_t> free_seqs;    // stack
+  int64_t fault_after = -1;          // fail the allocation that would exceed this count
+  int64_t allocated = 0;             // blocks handed out so far
+  // device mirror of the block table
+  int device = -1;
+  int32_t* d_table = nullptr;
+  std::vector<int32_t> h_table;
+  std::vector<uint8_t> dirty;
+  int64_t n_dirty = 0;
+  bool zeroed = false;
+
+  ~padoc_kv_pool() {
+    if (d_table) {
+      int cur = -1;
+      cudaGetDevice(&cur);
+      cudaSetDevice(device);
+      cudaFree(d_table);
+      if (cur >= 0) cudaSetDevice(cur);
+    }
+  }
+  bool seq_ok(int32_t s) const { return s >= 0 && s < max_seqs && seqs[s].live; }
+  int32_t own_blocks(const Seq& s) const { return static_cast<int32_t>(s.blocks.size()) - s.n_shared; }
+  void mark(int32_t s) {
+    if (!dirty[s]) {
+      dirty[s] = 1;
+      ++n_dirty;
+    }
+    int32_t* row = &h_table[static_cast<size_t>(s) * max_bps];
+    const Seq& q = seqs[s];
+    std::fill(row, row + max_bps, 0);
+    std::copy(q.blocks.begin(), q.blocks.end(), row);
+  }
+  // Takes n blocks or nothing.
+  bool take_blocks(int32_t n, std::vector<int32_t>* out) {
+    if (n < 0 || static_cast<size_t>(n) > free_blocks.size()) return false;
+    if (fault_after >= 0 && allocated + n > fault_after) return false;
+    for (int32_t i = 0; i < n; ++i) {
+      const int32_t b = free_blocks.back();
+      free_blocks.pop_back();
+      refcnt[b] = 1;
+      out->push_back(b);
+    }
+    allocated += n;
+    return true;
+  }
+  void drop_block(int32_t b) {
+    if (--refcnt[b] == 0) free_blocks.push_back(b);
+  }
+  int32_t new_seq() {
+    if (free_seqs.empty()) return -1;
+    const int32_t s = free_seqs.back();
+    free_seqs.pop_back();
+    seqs[s] = Seq();
+    seqs[s].live = true;
+    return s;
+  }
+};
+
+extern "C" int padoc_kv_pool_create(padoc_kv_pool** out, void* k_pool, void* v_pool, int32_t num_blocks,
+                                    int32_t block_size, int32_t Hkv, int32_t d, int32_t dtype,
+                                    int32_t max_seqs, int32_t max_blocks_per_seq) {
+  if (!out) return fail(PADOC_ERR_INVALID, "kv_pool_create: null out");
+  *out = nullptr;
+  if (block_size != 16) return fail(PADOC_ERR_UNSUPPORTED, "kv_pool_create: block_size must be 16");
+  if (d != 128) return fail(PADOC_ERR_UNSUPPORTED, "kv_pool_create: d must be 128");
+  if (dtype != PADOC_BF16) return fail(PADOC_ERR_UNSUPPORTED, "kv_pool_create: dtype must be bf16");
+  if (num_blocks <= 0 || Hkv <= 0 || max_seqs <= 0 || max_blocks_per_seq <= 0)
+    return fail(PADOC_ERR_INVALID, "kv_pool_create: sizes must be positive");
+  if (static_cast<int64_t>(num_blocks) * Hkv * block_size >= (int64_t(1) << 31))
+    return fail(PADOC_ERR_UNSUPPORTED, "kv_pool_create: num_blocks * Hkv * 16 must stay below 2^31");
+  if ((k_pool && !aligned16(k_pool)) || (v_pool && !aligned16(v_pool)))
+    return fail(PADOC_ERR_INVALID, "kv_pool_create: storage must be 16-byte aligned");
+  padoc_kv_pool* p = nullptr;
+  PADOC_TRY({
+    std::unique_ptr<padoc_kv_pool> pool(new padoc_kv_pool());
+    pool->k = k_pool;
+    pool->v = v_pool;
+    pool->nb = num_blocks;
+    pool->bs = block_size;
+    pool->Hkv = Hkv;
+    pool->d = d;
+    pool->dtype = dtype;
+    pool->max_seqs = max_seqs;
+    pool->max_bps = max_blocks_per_seq;
+    pool->refcnt.assign(num_blocks, 0);
+    pool->free_blocks.resize(num_blocks);
+    for (int32_t i = 0; i < num_blocks; ++i) pool->free_blocks[i] = num_blocks - 1 - i;
+    pool->seqs.resize(max_seqs);
+    pool->free_seqs.resize(max_seqs);
+    for (int32_t i = 0; i < max_seqs; ++i) pool->free_seqs[i] = max_seqs - 1 - i;
+    pool->h_table.assign(static_cast<size_t>(max_seqs) * max_blocks_per_seq, 0);
+    pool->dirty.assign(max_seqs, 0);
+    if (const char* f = std::getenv("PADOC_FAULT_ALLOC_AFTER")) pool->fault_after = std::atoll(f);
+    p = pool.release();
+  });
+  *out = p;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_pool_destroy(padoc_kv_pool* pool) {
+  delete pool;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_alloc(padoc_kv_pool* pool, int32_t n_tokens, int32_t* seq) {
+  if (!pool || !seq) return fail(PADOC_ERR_INVALID, "kv_alloc: null argument");
+  if (n_tokens < 0) return fail(PADOC_ERR_INVALID, "kv_alloc: n_tokens < 0");
+  const int32_t nblk = (n_tokens + pool->bs - 1) / pool->bs;
+  if (nblk > pool->max_bps) return fail(PADOC_ERR_INVALID, "kv_alloc: %d blocks exceed max_blocks_per_seq %d", nblk, pool->max_bps);
+  if (pool->free_seqs.empty()) return fail(PADOC_ERR_OOM, "kv_alloc: no free sequence slot");
+  std::vector<int32_t> blocks;
+  PADOC_TRY({
+    if (!pool->take_blocks(nblk, &blocks)) return fail(PADOC_ERR_OOM, "kv_alloc: out of blocks (%d wanted)", nblk);
+    const int32_t s = pool->new_seq();
+    pool->seqs[s].blocks = std::move(blocks);
+    pool->mark(s);
+    *seq = s;
+  });
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_fork(padoc_kv_pool* pool, int32_t parent, int32_t fork_len, int32_t* child) {
+  if (!pool || !child) return fail(PADOC_ERR_INVALID, "kv_fork: null argument");
+  if (!pool->seq_ok(parent)) return fail(PADOC_ERR_INVALID, "kv_fork: parent %d is not a live sequence", parent);
+  const Seq& par = pool->seqs[parent];
+  if (fork_len < 0 || fork_len > par.len)
+    return fail(PADOC_ERR_INVALID, "kv_fork: fork_len %d outside [0, %d]", fork_len, par.len);
+  // token t of the child (t < fork_len) must sit at block t/16, slot t%16 of the parent
+  if (fork_len > par.fork_len && par.fork_len % pool->bs != 0)
+    return fail(PADOC_ERR_UNSUPPORTED, "kv_fork: parent's own tokens do not start on a block boundary");
+  if (pool->free_seqs.empty()) return fail(PADOC_ERR_OOM, "kv_fork: no free sequence slot");
+  PADOC_TRY({
+    const int32_t nsh = (fork_len + pool->bs - 1) / pool->bs;
+    std::vector<int32_t> blocks(par.blocks.begin(), par.blocks.begin() + nsh);
+    const int32_t s = pool->new_seq();
+    for (int32_t b : blocks) ++pool->refcnt[b];
+    Seq& c = pool->seqs[s];
+    c.blocks = std::move(blocks);
+    c.len = fork_len;
+    c.fork_len = fork_len;
+    c.n_shared = nsh;
+    pool->mark(s);
+    *child = s;
+  });
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_release(padoc_kv_pool* pool, int32_t seq) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_release: null pool");
+  if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_release: %d is not a live sequence", seq);
+  Seq& s = pool->seqs[seq];
+  for (int32_t b : s.blocks) pool->drop_block(b);
+  s = Seq();
+  pool->mark(seq);
+  pool->free_seqs.push_back(seq);
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_seq_info(const padoc_kv_pool* pool, int32_t seq, int32_t* length, int32_t* fork_len,
+                                 int32_t* n_blocks) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_seq_info: null pool");
+  if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_seq_info: %d is not a live sequence", seq);
+  const Seq& s = pool->seqs[seq];
+  if (length) *length = s.len;
+  if (fork_len) *fork_len = s.fork_len;
+  if (n_blocks) *n_blocks = static_cast<int32_t>(s.blocks.size());
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_seq_blocks(const padoc_kv_pool* pool, int32_t seq, int32_t* out, int32_t cap) {
+  if (!pool || !out) return fail(PADOC_ERR_INVALID, "kv_seq_blocks: null argument");
+  if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_seq_blocks: %d is not a live sequence", seq);
+  const Seq& s = pool->seqs[seq];
+  if (cap < static_cast<int32_t>(s.blocks.size())) return fail(PADOC_ERR_INVALID, "kv_seq_blocks: capacity too small");
+  std::copy(s.blocks.begin(), s.blocks.end(), out);
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_block_refcount(const padoc_kv_pool* pool, int32_t block, int32_t* refcount) {
+  if (!pool || !refcount) return fail(PADOC_ERR_INVALID, "kv_block_refcount: null argument");
+  if (block < 0 || block >= pool->nb) return fail(PADOC_ERR_INVALID, "kv_block_refcount: block out of range");
+  *refcount = pool->refcnt[block];
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_pool_stats(const padoc_kv_pool* pool, int32_t* free_blocks, int32_t* live_seqs) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_pool_stats: null pool");
+  if (free_blocks) *free_blocks = static_cast<int32_t>(pool->free_blocks.size());
+  if (live_seqs) *live_seqs = pool->max_seqs - static_cast<int32_t>(pool->free_seqs.size());
+  return PADOC_OK;
+}
+
+static int pool_sync(padoc_kv_pool* pool, cudaStream_t stream) {
+  cudaError_t e;
+  if (!pool->d_table) {
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaMalloc(&pool->d_table, pool->h_table.size() * sizeof(int32_t));
+    if (e != cudaSuccess) {
+      pool->d_table = nullptr;
+      return cuda_fail(e, "kv pool table allocation");
+    }
+    pool->device = dev;
+    std::fill(pool->dirty.begin(), pool->dirty.end(), 1);
+    pool->n_dirty = pool->max_seqs;
+  }
+  if (!pool->zeroed && pool->k && pool->v) {
+    // Unwritten slots of a partly filled block are read (and masked) by the
+    // kernels; zeroing once keeps them finite.
+    const size_t bytes = static_cast<size_t>(pool->nb) * pool->Hkv * pool->bs * pool->d * 2;
+    e = cudaMemsetAsync(pool->k, 0, bytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(pool->v, 0, bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kv pool zero fill");
+    pool->zeroed = true;
+  }
+  if (pool->n_dirty == 0) return PADOC_OK;
+  const size_t row = static_cast<size_t>(pool->max_bps);
+  if (pool->n_dirty > 64) {
+    int32_t lo = pool->max_seqs, hi = -1;
+    for (int32_t s = 0; s < pool->max_seqs; ++s)
+      if (pool->dirty[s]) {
+        lo = std::min(lo, s);
+        hi = std::max(hi, s);
+      }
+    e = cudaMemcpyAsync(pool->d_table + lo * row, pool->h_table.data() + lo * row,
+                        (hi - lo + 1) * row * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kv pool table upload");
+  } else {
+    for (int32_t s = 0; s < pool->max_seqs; ++s)
+      if (pool->dirty[s]) {
+        e = cudaMemcpyAsync(pool->d_table + s * row, pool->h_table.data() + s * row, row * sizeof(int32_t),
+                            cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kv pool table upload");
+      }
+  }
+  std::fill(pool->dirty.begin(), pool->dirty.end(), 0);
+  pool->n_dirty = 0;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_pool_sync(padoc_kv_pool* pool, padoc_stream_t stream) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_pool_sync: null pool");
+  return pool_sync(pool, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int padoc_kv_append(padoc_kv_pool* pool, int32_t seq, const void* k, const void* v, int32_t n,
+                               padoc_stream_t stream) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_append: null pool");
+  if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_append: %d is not a live sequence", seq);
+  if (n < 0) return fail(PADOC_ERR_INVALID, "kv_append: n < 0");
+  if (n == 0) return PADOC_OK;
+  if (!k || !v || !aligned16(k) || !aligned16(v)) return fail(PADOC_ERR_INVALID, "kv_append: k/v must be 16-byte aligned device pointers");
+  if (!pool->k || !pool->v) return fail(PADOC_ERR_INVALID, "kv_append: pool has no storage");
+  Seq& s = pool->seqs[seq];
+  const int32_t own = s.len - s.fork_len;
+  const int64_t need_tokens = static_cast<int64_t>(own) + n;
+  const int64_t need_blocks = (need_tokens + pool->bs - 1) / pool->bs;
+  const int64_t have = pool->own_blocks(s);
+  if (s.n_shared + need_blocks > pool->max_bps)
+    return fail(PADOC_ERR_INVALID, "kv_append: sequence would exceed max_blocks_per_seq");
+  if (need_blocks > have) {
+    std::vector<int32_t> extra;
+    PADOC_TRY({
+      if (!pool->take_blocks(static_cast<int32_t>(need_blocks - have), &extra))
+        return fail(PADOC_ERR_OOM, "kv_append: out of blocks");
+      s.blocks.insert(s.blocks.end(), extra.begin(), extra.end());
+    });
+  }
+  s.len += n;
+  pool->mark(seq);
+  int rc = pool_sync(pool, reinterpret_cast<cudaStream_t>(stream));
+  if (rc) return rc;
+  std::string err;
+  rc = launch_kv_append(pool->k, pool->v, pool->d_table + static_cast<size_t>(seq) * pool->max_bps + s.n_shared, own, n,
+                        pool->Hkv, pool->d, k, v, reinterpret_cast<cudaStream_t>(stream), &err);
+  if (rc) return fail(rc, "kv_append: %s", err.c_str());
+  return PADOC_OK;
+}
+
+// ============================================================== decode planning
+
+namespace {
+
+struct DecodePlan {
+  std::vector<DecPage> pages;
+  std::vector<DecItem> items;
+  std::vector<DecBranch> branches;
+  std::vector<int32_t> q_plen;
+  int64_t part_rows = 0;
+  size_t off_pages = 0, off_items = 0, off_branches = 0, off_qplen = 0, off_part_o = 0, off_part_lse = 0,
+         total = 0;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t Hq, int n_sms, DecodePlan* pl) {
+  if (!pool || !b) return fail(PADOC_ERR_INVALID, "branch_decode: null argument");
+  if (Hq <= 0 || Hq % pool->Hkv != 0)
+    return fail(PADOC_ERR_INVALID, "branch_decode: Hq=%d must be a positive multiple of Hkv=%d", Hq, pool->Hkv);
+  const int G = Hq / pool->Hkv;
+  if (G > 8) return fail(PADOC_ERR_UNSUPPORTED, "branch_decode: Hq/Hkv=%d above 8", G);
+  if (b->n_pages < 0 || b->n_branches < 0) return fail(PADOC_ERR_INVALID, "branch_decode: negative counts");
+  if (b->n_pages > 0 && (!b->page_seq || !b->branch_offsets))
+    return fail(PADOC_ERR_INVALID, "branch_decode: null page arrays");
+  if (b->n_branches > 0 && (!b->branch_seq || !b->q_offsets))
+    return fail(PADOC_ERR_INVALID, "branch_decode: null branch arrays");
+  if (b->n_pages == 0 && b->n_branches > 0) return fail(PADOC_ERR_INVALID, "branch_decode: branches without pages");
+  if (b->n_pages > 0) {
+    if (b->branch_offsets[0] != 0 || b->branch_offsets[b->n_pages] != b->n_branches)
+      return fail(PADOC_ERR_INVALID, "branch_decode: branch_offsets must run from 0 to n_branches");
+  }
+  if (b->n_branches > 0 && b->q_offsets[0] != 0) return fail(PADOC_ERR_INVALID, "branch_decode: q_offsets[0] != 0");
+  for (int32_t i = 0; i < b->n_branches; ++i) {
+    const int32_t ql = b->q_offsets[i + 1] - b->q_offsets[i];
+    if (ql < 1 || ql > 16) return fail(PADOC_ERR_INVALID, "branch_decode: branch %d has %d query rows (1..16)", i, ql);
+  }
+  const int32_t nq = b->n_branches ? b->q_offsets[b->n_branches] : 0;
+  pl->q_plen.assign(nq, 0);
+  pl->branches.resize(b->n_branches);
+  pl->pages.resize(b->n_pages);
+  // chunk length from the total prefix work, so items fill the GPU
+  int64_t work_tiles = 0;
+  std::vector<int32_t> P(b->n_pages, 0);
+  for (int32_t p = 0; p < b->n_pages; ++p) {
+    const int32_t ps = b->page_seq[p];
+    if (!pool->seq_ok(ps)) return fail(PADOC_ERR_INVALID, "branch_decode: page %d sequence %d not live", p, ps);
+    const Seq& pseq = pool->seqs[ps];
+    const int32_t b0 = b->branch_offsets[p], b1 = b->branch_offsets[p + 1];
+    if (b1 < b0) return fail(PADOC_ERR_INVALID, "branch_decode: branch_offsets not ascending");
+    for (int32_t i = b0; i < b1; ++i) {
+      const int32_t s = b->branch_seq[i];
+      if (!pool->seq_ok(s)) return fail(PADOC_ERR_INVALID, "branch_decode: branch %d sequence %d not live", i, s);
+      const Seq& bs = pool->seqs[s];
+      if (bs.fork_len > pseq.len)
+        return fail(PADOC_ERR_INVALID, "branch_decode: branch %d sees %d prefix tokens, page has %d", i, bs.fork_len, pseq.len);
+      if (bs.fork_len > pseq.fork_len && pseq.fork_len % pool->bs != 0)
+        return fail(PADOC_ERR_UNSUPPORTED, "branch_decode: page %d prefix is not block aligned", p);
+      for (int32_t j = 0; j < bs.n_shared; ++j)
+        if (j >= static_cast<int32_t>(pseq.blocks.size()) || bs.blocks[j] != pseq.blocks[j])
+          return fail(PADOC_ERR_INVALID, "branch_decode: branch %d is not a fork of page %d's sequence", i, p);
+      P[p] = std::max(P[p], bs.fork_len);
+    }
+    const int32_t nqp = (b1 > b0) ? b->q_offsets[b1] - b->q_offsets[b0] : 0;
+    const int32_t rt = (nqp * G + kTileRows - 1) / kTileRows;
+    work_tiles += static_cast<int64_t>(rt) * ((P[p] + kTileKeys - 1) / kTileKeys) * pool->Hkv;
+  }
+  int64_t ct = work_tiles / (2 * static_cast<int64_t>(n_sms));
+  ct = std::max<int64_t>(8, std::min<int64_t>(40, ct));
+  int64_t rows = 0;
+  for (int32_t p = 0; p < b->n_pages; ++p) {
+    const int32_t b0 = b->branch_offsets[p], b1 = b->branch_offsets[p + 1];
+    DecPage& pg = pl->pages[p];
+    pg.seq = b->page_seq[p];
+    pg.P = P[p];
+    pg.q_first = (b1 > b0) ? b->q_offsets[b0] : 0;
+    pg.nq = (b1 > b0) ? b->q_offsets[b1] - b->q_offsets[b0] : 0;
+    pg.row_tiles = (pg.nq * G + kTileRows - 1) / kTileRows;
+    const int32_t tiles = (pg.P + kTileKeys - 1) / kTileKeys;
+    pg.n_chunks = (tiles == 0 || pg.nq == 0) ? 0 : static_cast<int32_t>((tiles + ct - 1) / ct);
+    pg.chunk_tokens = pg.n_chunks ? ((tiles + pg.n_chunks - 1) / pg.n_chunks) * kTileKeys : 0;
+    pg.n_chunks = pg.chunk_tokens ? (pg.P + pg.chunk_tokens - 1) / pg.chunk_tokens : 0;
+    pg.item_base = static_cast<int32_t>(pl->items.size());
+    for (int32_t t = 0; t < pg.row_tiles && pg.n_chunks; ++t)
+      for (int32_t c = 0; c < pg.n_chunks; ++c) {
+        DecItem it{};
+        it.page = p;
+        it.tile = t;
+        it.chunk = c;
+        it.rows = std::min(kTileRows, pg.nq * G - t * kTileRows);
+        it.row_base = static_cast<int32_t>(rows);
+        rows += static_cast<int64_t>(it.rows) * pool->Hkv;
+        pl->items.push_back(it);
+      }
+    for (int32_t i = b0; i < b1; ++i) {
+      const Seq& bs = pool->seqs[b->branch_seq[i]];
+      DecBranch& br = pl->branches[i];
+      br.page = p;
+      br.seq = b->branch_seq[i];
+      br.prefix_len = bs.fork_len;
+      br.own_len = bs.len - bs.fork_len;
+      br.n_shared = bs.n_shared;
+      br.q_first = b->q_offsets[i];
+      br.q_len = b->q_offsets[i + 1] - b->q_offsets[i];
+      br.q_in_page = br.q_first - pg.q_first;
+      for (int32_t r = br.q_first; r < br.q_first + br.q_len; ++r) pl->q_plen[r] = br.prefix_len;
+    }
+  }
+  if (rows >= (int64_t(1) << 31)) return fail(PADOC_ERR_UNSUPPORTED, "branch_decode: batch too large");
+  pl->part_rows = rows;
+  size_t off = 0;
+  pl->off_pages = off;
+  off = align_up(off + pl->pages.size() * sizeof(DecPage), 256);
+  pl->off_items = off;
+  off = align_up(off + pl->items.size() * sizeof(DecItem), 256);
+  pl->off_branches = off;
+  off = align_up(off + pl->branches.size() * sizeof(DecBranch), 256);
+  pl->off_qplen = off;
+  off = align_up(off + pl->q_plen.size() * sizeof(int32_t), 256);
+  pl->off_part_o = off;
+  off = align_up(off + static_cast<size_t>(rows) * kHeadDim * sizeof(float), 256);
+  pl->off_part_lse = off;
+  off = align_up(off + static_cast<size_t>(rows) * sizeof(float), 256);
+  pl->total = off;
+  return PADOC_OK;
+}
+
+}  // namespace
+
+extern "C" int padoc_branch_decode_ws_size(const padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq,
+                                           size_t* bytes) {
+  if (!bytes) return fail(PADOC_ERR_INVALID, "branch_decode_ws_size: null bytes");
+  DecodePlan pl;
+  int rc;
+  PADOC_TRY(rc = plan_decode(pool, batch, Hq, num_sms(), &pl));
+  if (rc) return rc;
+  *bytes = pl.total;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq, const void* q,
+                                   const void* k_new, const void* v_new, const uint16_t* tree_bits, void* o,
+                                   float* lse, float scale, void* ws, size_t ws_bytes, padoc_stream_t stream) {
+  DecodePlan pl;
+  int rc;
+  PADOC_TRY(rc = plan_decode(pool, batch, Hq, num_sms(), &pl));
+  if (rc) return rc;
+  if (batch->n_branches == 0) return PADOC_OK;
+  if (!q || !k_new || !v_new || !o || !lse || !ws) return fail(PADOC_ERR_INVALID, "branch_decode: null tensor");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(o) || !aligned16(lse))
+    return fail(PADOC_ERR_INVALID, "branch_decode: tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(PADOC_ERR_INVALID, "branch_decode: ws must be 256-byte aligned");
+  if (ws_bytes < pl.total) return fail(PADOC_ERR_INVALID, "branch_decode: workspace %zu bytes, need %zu", ws_bytes, pl.total);
+  if (!pool->k || !pool->v) return fail(PADOC_ERR_INVALID, "branch_decode: pool has no storage");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = pool_sync(pool, st);
+  if (rc) return rc;
+  // one host buffer holding the plan arrays, copied in one transfer
+  std::vector<uint8_t> host;
+  PADOC_TRY(host.assign(pl.off_part_o, 0));
+  std::memcpy(host.data() + pl.off_pages, pl.pages.data(), pl.pages.size() * sizeof(DecPage));
+  std::memcpy(host.data() + pl.off_items, pl.items.data(), pl.items.size() * sizeof(DecItem));
+  std::memcpy(host.data() + pl.off_branches, pl.branches.data(), pl.branches.size() * sizeof(DecBranch));
+  std::memcpy(host.data() + pl.off_qplen, pl.q_plen.data(), pl.q_plen.size() * sizeof(int32_t));
+  cudaError_t e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "branch_decode: plan upload");
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  DecodeArgs a;
+  a.pages = reinterpret_cast<const DecPage*>(w + pl.off_pages);
+  a.items = reinterpret_cast<const DecItem*>(w + pl.off_items);
+  a.branches = reinterpret_cast<const DecBranch*>(w + pl.off_branches);
+  a.q_plen = reinterpret_cast<const int32_t*>(w + pl.off_qplen);
+  a.table = pool->d_table;
+  a.max_bps = pool->max_bps;
+  a.n_pages = batch->n_pages;
+  a.n_items = static_cast<int32_t>(pl.items.size());
+  a.n_branches = batch->n_branches;
+  a.nq = static_cast<int32_t>(pl.q_plen.size());
+  a.Hq = Hq;
+  a.Hkv = pool->Hkv;
+  a.group = Hq / pool->Hkv;
+  a.d = pool->d;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(pool->d));
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.tree_bits = tree_bits;
+  a.o = o;
+  a.lse = lse;
+  a.part_o = reinterpret_cast<float*>(w + pl.off_part_o);
+  a.part_lse = reinterpret_cast<float*>(w + pl.off_part_lse);
+  a.k_pool = pool->k;
+  a.v_pool = pool->v;
+  a.num_blocks = pool->nb;
+  std::string err;
+  if (a.n_items > 0) {
+    rc = launch_decode_prefix(a, st, &err);
+    if (rc) return fail(rc, "branch_decode: %s", err.c_str());
+  }
+  rc = launch_decode_own(a, st, &err);
+  if (rc) return fail(rc, "branch_decode: %s", err.c_str());
+  return PADOC_OK;
+}
+
+// ============================================================== small host helpers
+
+extern "C" int padoc_tree_mask_build(const int32_t* parent, int32_t n, uint16_t* bits) {
+  if (n < 0 || n > 16) return fail(PADOC_ERR_INVALID, "tree_mask_build: n=%d outside [0, 16]", n);
+  if (n > 0 && (!parent || !bits)) return fail(PADOC_ERR_INVALID, "tree_mask_build: null argument");
+  for (int32_t i = 0; i < n; ++i)
+    if (parent[i] >= i || parent[i] < -1)
+      return fail(PADOC_ERR_INVALID, "tree_mask_build: parent[%d]=%d must be -1 or an earlier node", i, parent[i]);
+  for (int32_t i = 0; i < n; ++i) {
+    const uint16_t up = parent[i] >= 0 ? bits[parent[i]] : 0;
+    bits[i] = static_cast<uint16_t>(up | (1u << i));
+  }
+  return PADOC_OK;
+}
+
+extern "C" int padoc_depths(const int32_t* layout_len, const int32_t* content_len, int32_t n_regions,
+                            int64_t* d_seq, int64_t* d_tree) {
+  if (n_regions < 0) return fail(PADOC_ERR_INVALID, "depths: n_regions < 0");
+  if (n_regions > 0 && (!layout_len || !content_len)) return fail(PADOC_ERR_INVALID, "depths: null arrays");
+  int64_t seq = 0, tree = 0, acc = 0;
+  for (int32_t k = 0; k < n_regions; ++k) {
+    if (layout_len[k] < 0 || content_len[k] < 0) return fail(PADOC_ERR_INVALID, "depths: negative length");
+    acc += layout_len[k];
+    seq += layout_len[k] + content_len[k];
+    tree = std::max(tree, acc + content_len[k]);
+  }
+  if (d_seq) *d_seq = seq;
+  if (d_tree) *d_tree = tree;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_device_status(padoc_stream_t stream) {
+  unsigned w = 0;
+  const int rc = read_and_clear_tc_error(reinterpret_cast<cudaStream_t>(stream), &w);
+  if (rc) return fail(rc, "device_status: could not read the device error word");
+  if (w) return fail(PADOC_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (site mask 0x%x)", w);
+  return PADOC_OK;
+}

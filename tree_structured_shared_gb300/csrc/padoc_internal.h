@@ -1,0 +1,120 @@
+// Structures shared by the host library and the kernel launchers.
+#pragma once
+#include <cstdint>
+#include <string>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace padoc {
+
+// ---------------------------------------------------------------- forward
+// A query segment: packed positions [q_start, q_start + q_len) that share one
+// ordered list of key/value segments kvsegs[kv_first .. kv_first + kv_count).
+struct QSeg {
+  int32_t q_start, q_len, kv_first, kv_count;
+};
+// Keys [start, start + len); when causal, a query at packed position t sees
+// only keys <= t (all keys of the segment before the query are visible).
+struct KVSeg {
+  int32_t start, len, causal, pad;
+};
+// One query tile: tile_tokens consecutive tokens of one query segment.
+struct FwdItem {
+  int32_t qseg, tile_start;
+};
+
+constexpr int kTileKeys = 128;  // keys per K/V tile
+constexpr int kTileRows = 128;  // MMA M: query rows (tokens x heads of a GQA group)
+constexpr int kHeadDim = 128;   // d of the tensor-core path
+
+struct FwdPlan {
+  const QSeg* qsegs;
+  const KVSeg* kvsegs;
+  const FwdItem* items;
+  int32_t n_items;
+  int32_t group;        // Hq / Hkv
+  int32_t tile_tokens;  // kTileRows / group
+};
+
+struct FwdArgs {
+  FwdPlan plan;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int64_t T;
+  int32_t Hq, Hkv, d;
+  float scale;
+};
+
+// ---------------------------------------------------------------- decode
+struct DecPage {
+  int32_t seq;           // block-table row holding the shared prefix
+  int32_t P;             // prefix tokens any branch of the page sees
+  int32_t q_first;       // first query row of the page
+  int32_t nq;            // query rows of the page
+  int32_t item_base;     // first prefix item of the page
+  int32_t n_chunks;      // prefix chunks
+  int32_t chunk_tokens;  // tokens per chunk (multiple of kTileKeys)
+  int32_t row_tiles;     // ceil(nq * group / kTileRows)
+};
+struct DecItem {
+  int32_t page, tile, chunk;
+  int32_t rows;      // valid rows of this row tile
+  int32_t row_base;  // partial row index of head 0; head g adds g * rows
+  int32_t pad[3];
+};
+struct DecBranch {
+  int32_t page, seq;
+  int32_t prefix_len;  // shared prefix tokens this branch sees
+  int32_t own_len;     // own cached tokens
+  int32_t n_shared;    // leading blocks of seq that belong to the prefix
+  int32_t q_first, q_len;
+  int32_t q_in_page;   // index of its first query among its page's queries
+};
+
+struct DecodeArgs {
+  const DecPage* pages;
+  const DecItem* items;
+  const DecBranch* branches;
+  const int32_t* q_plen;  // [nq] prefix tokens visible to each query row
+  const int32_t* table;   // device block table [max_seqs][max_bps]
+  int32_t max_bps;
+  int32_t n_pages, n_items, n_branches, nq;
+  int32_t Hq, Hkv, group, d;
+  float scale;
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const uint16_t* tree_bits;
+  void* o;
+  float* lse;
+  float* part_o;    // [rows][d] f32 normalised partial outputs of the prefix pass
+  float* part_lse;  // [rows] f32
+  const void* k_pool;
+  const void* v_pool;
+  int64_t num_blocks;
+};
+
+// Launchers (return 0 or a PADOC_ERR_* code, message in *err).
+int launch_fwd_bf16(const FwdArgs& a, cudaStream_t s, std::string* err);
+int launch_fwd_f32(const FwdArgs& a, cudaStream_t s, std::string* err);
+int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err);
+int launch_decode_own(const DecodeArgs& a, cudaStream_t s, std::string* err);
+int launch_kv_append(void* k_pool, void* v_pool, const int32_t* table_row, int32_t first_own,
+                     int32_t n, int32_t Hkv, int32_t d, const void* k, const void* v,
+                     cudaStream_t s, std::string* err);
+
+// Device error words (set by kernels that give up a bounded wait).
+int read_and_clear_tc_error(cudaStream_t s, unsigned* word);
+
+// Driver entry point for tensor-map encoding (resolved through the runtime).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_fn(std::string* err);
+int num_sms();
+
+}  // namespace padoc

@@ -1,0 +1,194 @@
+"""Puts seeded workloads on the GPU and runs them through libpadoc.
+
+Used by the GPU tests and by bench.py.  Holds no attention arithmetic: it
+allocates device tensors, fills the KV pool through padoc_kv_append, builds the
+decode batch arrays, and calls the C ABI.
+"""
+from __future__ import annotations
+
+import dataclasses
+import zlib
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+from . import padoc
+from . import workloads as wl
+
+
+def _bf16(x: np.ndarray, device) -> torch.Tensor:
+    """Exactly representable float32 values -> device bf16 (lossless)."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device).to(torch.bfloat16)
+
+
+# ------------------------------------------------------------------ forward
+
+
+class Forward:
+    """A tree-varlen forward over packed pages with inputs resident on the GPU."""
+
+    def __init__(self, w: wl.TreeWorkload, q=None, k=None, v=None, order: int = padoc.PACK_CANONICAL,
+                 device="cuda", seed: int = 0):
+        self.w = w
+        self.desc = padoc.TreeDesc(w.pages, order)
+        T = w.n_tokens
+        self.T = T
+        self.dtype = padoc.BF16 if w.dtype == "bf16" else padoc.F32
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        if q is None:
+            g = torch.Generator(device=device)
+            g.manual_seed(seed)
+            self.q = (torch.randn(T, w.Hq, w.d, device=device, generator=g) * w.value_scale).to(tdt)
+            self.k = (torch.randn(T, w.Hkv, w.d, device=device, generator=g) * w.value_scale).to(tdt)
+            self.v = (torch.randn(T, w.Hkv, w.d, device=device, generator=g) * w.value_scale).to(tdt)
+        else:
+            conv = (lambda a: _bf16(a, device)) if w.dtype == "bf16" else (
+                lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device))
+            self.q, self.k, self.v = conv(q), conv(k), conv(v)
+        self.o = torch.empty(max(T, 1), w.Hq, w.d, dtype=tdt, device=device)
+        self.lse = torch.empty(w.Hq, max(T, 1), dtype=torch.float32, device=device)
+        self.desc.upload(w.Hq // w.Hkv)
+
+    def run(self, stream=None):
+        padoc.tree_attn_varlen(self.desc, self.q, self.k, self.v, self.o, self.lse, self.dtype, self.w.Hq,
+                               self.w.Hkv, self.w.d, 0.0, stream)
+        return self.o, self.lse
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic flops: 4 d Hq per (query, ancestor) pair."""
+        return 4.0 * self.w.d * self.w.Hq * self.desc.info()["ancestor_pairs"]
+
+
+# ------------------------------------------------------------------ decode
+
+
+def _seed(*parts) -> int:
+    return zlib.crc32(repr(parts).encode()) & 0x7FFFFFFF
+
+
+@dataclasses.dataclass
+class DeviceDecodeValues:
+    """Per-item seeded device values; any item can be regenerated alone."""
+
+    w: wl.DecodeWorkload
+    seed: int
+    device: str
+
+    def _randn(self, tag, idx, shape):
+        g = torch.Generator(device=self.device)
+        g.manual_seed(_seed(self.seed, tag, idx))
+        x = torch.randn(*shape, device=self.device, generator=g) * self.w.value_scale
+        return x.to(torch.bfloat16)
+
+    def prefix(self, p):
+        P = self.w.pages[p].prefix_len
+        return (self._randn("pk", p, (P, self.w.Hkv, self.w.d)), self._randn("pv", p, (P, self.w.Hkv, self.w.d)))
+
+    def own(self, b, L):
+        return (self._randn("ok", b, (L, self.w.Hkv, self.w.d)), self._randn("ov", b, (L, self.w.Hkv, self.w.d)))
+
+    def block(self, nq):
+        return (self._randn("q", 0, (nq, self.w.Hq, self.w.d)), self._randn("kn", 0, (nq, self.w.Hkv, self.w.d)),
+                self._randn("vn", 0, (nq, self.w.Hkv, self.w.d)))
+
+
+class Decode:
+    """A branch-decode / verify step: pool filled with each page's prefix and
+    each branch's own suffix (a zero-copy fork of its page), plus the query
+    block, all resident on the GPU."""
+
+    def __init__(self, w: wl.DecodeWorkload, vals: Optional[wl.DecodeValues] = None, seed: int = 0,
+                 device="cuda", tree: bool = True, slack_blocks: int = 8):
+        self.w = w
+        Hkv, d = w.Hkv, w.d
+        nb = sum((p.prefix_len + 15) // 16 for p in w.pages)
+        nb += sum((L + 15) // 16 for p in w.pages for L in p.own_len) + slack_blocks
+        max_bps = max([(p.prefix_len + 15) // 16 + (max(p.own_len or [0]) + 15) // 16 + 2 for p in w.pages] + [4])
+        self.k_pool = torch.empty(nb, Hkv, 16, d, dtype=torch.bfloat16, device=device)
+        self.v_pool = torch.empty(nb, Hkv, 16, d, dtype=torch.bfloat16, device=device)
+        self.pool = padoc.KVPool(self.k_pool, self.v_pool, nb, Hkv, d,
+                                 max_seqs=len(w.pages) + w.n_branches + 8, max_blocks_per_seq=max_bps)
+        self.pool.sync()
+        self.gen = DeviceDecodeValues(w, seed, device) if vals is None else None
+        page_seq, branch_seq, boff, qoff = [], [], [0], [0]
+        b = 0
+        for p, pg in enumerate(w.pages):
+            s = self.pool.alloc(pg.prefix_len)
+            if pg.prefix_len:
+                if vals is not None:
+                    k, v = _bf16(vals.prefix_k[p], device), _bf16(vals.prefix_v[p], device)
+                else:
+                    k, v = self.gen.prefix(p)
+                self.pool.append(s, k, v, pg.prefix_len)
+            page_seq.append(s)
+            for j in range(len(pg.own_len)):
+                c = self.pool.fork(s, pg.branch_prefix_len[j])
+                L = pg.own_len[j]
+                if L:
+                    if vals is not None:
+                        k, v = _bf16(vals.own_k[b], device), _bf16(vals.own_v[b], device)
+                    else:
+                        k, v = self.gen.own(b, L)
+                    self.pool.append(c, k, v, L)
+                branch_seq.append(c)
+                qoff.append(qoff[-1] + pg.q_len[j])
+                b += 1
+            boff.append(len(branch_seq))
+        self.page_seq, self.branch_seq = page_seq, branch_seq
+        self.batch = padoc.Batch(page_seq, boff, branch_seq, qoff)
+        nq = qoff[-1]
+        self.nq = nq
+        if vals is not None:
+            self.q, self.k_new, self.v_new = (_bf16(vals.q, device), _bf16(vals.k_new, device),
+                                              _bf16(vals.v_new, device))
+        else:
+            self.q, self.k_new, self.v_new = self.gen.block(nq)
+        if tree:
+            bits = np.concatenate([padoc.tree_mask_build(par) for pg in w.pages for par in pg.parents])
+            self.tree_bits = torch.from_numpy(bits.astype(np.int16)).to(device)
+        else:
+            self.tree_bits = None
+        self.ws_bytes = padoc.branch_decode_ws_size(self.pool, self.batch, w.Hq)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.o = torch.empty(max(nq, 1), w.Hq, d, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(max(nq, 1), w.Hq, dtype=torch.float32, device=device)
+        torch.cuda.synchronize()
+
+    def run(self, stream=None):
+        padoc.branch_decode(self.pool, self.batch, self.w.Hq, self.q, self.k_new, self.v_new, self.tree_bits,
+                            self.o, self.lse, self.ws, self.ws_bytes, 0.0, stream)
+        return self.o, self.lse
+
+    def unique_kv_bytes(self) -> int:
+        """Algorithmic bytes of one step: each shared prefix token once per
+        page (the longest prefix any of its branches sees), each own token
+        once, the query block's K/V, Q in, O and LSE out."""
+        w = self.w
+        row = w.Hkv * w.d * 2 * 2
+        toks = sum(max(p.branch_prefix_len or [0]) + sum(p.own_len) for p in w.pages)
+        nq = self.nq
+        return toks * row + nq * row + nq * w.Hq * w.d * 2 * 2 + nq * w.Hq * 4
+
+    def flops(self) -> float:
+        w = self.w
+        pairs = 0
+        for pg in w.pages:
+            for j in range(len(pg.own_len)):
+                nb = pg.q_len[j]
+                bits = padoc.tree_mask_build(pg.parents[j]) if self.tree_bits is not None else None
+                inblock = sum(bin(int(x)).count("1") for x in bits) if bits is not None else nb * (nb + 1) // 2
+                pairs += nb * (pg.branch_prefix_len[j] + pg.own_len[j]) + inblock
+        return 4.0 * w.d * w.Hq * pairs
+
+    def host_values(self, p: int) -> dict:
+        """Host copies of page p's inputs (from the seeded generator, not the
+        pool), for checking sampled rows against the oracle."""
+        assert self.gen is not None
+        pk, pv = self.gen.prefix(p)
+        b0 = sum(len(pg.own_len) for pg in self.w.pages[:p])
+        own = [self.gen.own(b0 + j, L) for j, L in enumerate(self.w.pages[p].own_len)]
+        return {"prefix_k": pk.float().cpu().numpy(), "prefix_v": pv.float().cpu().numpy(),
+                "own_k": [o[0].float().cpu().numpy() for o in own],
+                "own_v": [o[1].float().cpu().numpy() for o in own]}

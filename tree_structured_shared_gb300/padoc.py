@@ -1,0 +1,298 @@
+"""ctypes binding over libpadoc.so: argument marshalling only.
+
+Every computation runs in the library's CUDA kernels.  The names mirror the C
+functions declared in include/padoc.h.  Tensors may be torch tensors (their
+data_ptr() is passed) or raw integer device addresses.  There is no CPU path:
+if the compiled library is missing, loading fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpadoc.so")
+
+OK, ERR_INVALID, ERR_OOM, ERR_CUDA, ERR_UNSUPPORTED, ERR_DEVICE_TIMEOUT = 0, -1, -2, -3, -4, -5
+F32, BF16 = 0, 1
+PACK_CANONICAL, PACK_DOCUMENT = 0, 1
+
+EXPORTED = [
+    "padoc_last_error", "padoc_version", "padoc_tree_desc_build", "padoc_tree_desc_free",
+    "padoc_tree_desc_info", "padoc_tree_desc_segments", "padoc_tree_desc_upload",
+    "padoc_tree_attn_varlen", "padoc_kv_pool_create", "padoc_kv_pool_destroy", "padoc_kv_alloc",
+    "padoc_kv_append", "padoc_kv_fork", "padoc_kv_release", "padoc_kv_seq_info", "padoc_kv_seq_blocks",
+    "padoc_kv_block_refcount", "padoc_kv_pool_stats", "padoc_kv_pool_sync",
+    "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
+    "padoc_device_status",
+]
+
+
+class PadocError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libpadoc error {code}: {msg}")
+        self.code = code
+
+
+class TreeSpec(C.Structure):
+    _fields_ = [("n_pages", C.c_int32), ("prefix_len", C.POINTER(C.c_int32)),
+                ("n_regions", C.POINTER(C.c_int32)), ("layout_len", C.POINTER(C.c_int32)),
+                ("content_len", C.POINTER(C.c_int32)), ("order", C.c_int32)]
+
+
+class DecodeBatch(C.Structure):
+    _fields_ = [("n_pages", C.c_int32), ("n_branches", C.c_int32), ("page_seq", C.POINTER(C.c_int32)),
+                ("branch_offsets", C.POINTER(C.c_int32)), ("branch_seq", C.POINTER(C.c_int32)),
+                ("q_offsets", C.POINTER(C.c_int32))]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Loads libpadoc.so (built by tree_structured_shared_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run tree_structured_shared_gb300.build first")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, i64, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_float
+        p32, p64 = C.POINTER(C.c_int32), C.POINTER(C.c_int64)
+        sig = {
+            "padoc_last_error": (C.c_char_p, []),
+            "padoc_version": (C.c_int, []),
+            "padoc_tree_desc_build": (C.c_int, [C.POINTER(TreeSpec), C.POINTER(vp)]),
+            "padoc_tree_desc_free": (C.c_int, [vp]),
+            "padoc_tree_desc_info": (C.c_int, [vp, p64, p64, p64, p64]),
+            "padoc_tree_desc_segments": (C.c_int, [vp, p32, p32]),
+            "padoc_tree_desc_upload": (C.c_int, [vp, i32]),
+            "padoc_tree_attn_varlen": (C.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, vp]),
+            "padoc_kv_pool_create": (C.c_int, [C.POINTER(vp), vp, vp, i32, i32, i32, i32, i32, i32, i32]),
+            "padoc_kv_pool_destroy": (C.c_int, [vp]),
+            "padoc_kv_alloc": (C.c_int, [vp, i32, p32]),
+            "padoc_kv_append": (C.c_int, [vp, i32, vp, vp, i32, vp]),
+            "padoc_kv_fork": (C.c_int, [vp, i32, i32, p32]),
+            "padoc_kv_release": (C.c_int, [vp, i32]),
+            "padoc_kv_seq_info": (C.c_int, [vp, i32, p32, p32, p32]),
+            "padoc_kv_seq_blocks": (C.c_int, [vp, i32, p32, i32]),
+            "padoc_kv_block_refcount": (C.c_int, [vp, i32, p32]),
+            "padoc_kv_pool_stats": (C.c_int, [vp, p32, p32]),
+            "padoc_kv_pool_sync": (C.c_int, [vp, vp]),
+            "padoc_branch_decode_ws_size": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, C.POINTER(C.c_size_t)]),
+            "padoc_branch_decode": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, vp, vp, vp, vp, vp, vp, f32, vp,
+                                              C.c_size_t, vp]),
+            "padoc_tree_mask_build": (C.c_int, [p32, i32, C.POINTER(C.c_uint16)]),
+            "padoc_depths": (C.c_int, [p32, p32, i32, p64, p64]),
+            "padoc_device_status": (C.c_int, [vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != OK:
+        raise PadocError(rc, lib().padoc_last_error().decode(errors="replace"))
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream or None
+        except Exception:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p32(a: np.ndarray):
+    return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+# ------------------------------------------------------------------ tree descriptor
+
+
+class TreeDesc:
+    """Host descriptor of packed pages (padoc_tree_desc_build)."""
+
+    def __init__(self, pages, order: int = PACK_CANONICAL):
+        self._keep = [
+            _i32([p.prefix_len for p in pages]),
+            _i32([len(p.layout_len) for p in pages]),
+            _i32([x for p in pages for x in p.layout_len] or [0]),
+            _i32([x for p in pages for x in p.content_len] or [0]),
+        ]
+        spec = TreeSpec(len(pages), _p32(self._keep[0]), _p32(self._keep[1]), _p32(self._keep[2]),
+                        _p32(self._keep[3]), order)
+        h = C.c_void_p()
+        _check(lib().padoc_tree_desc_build(C.byref(spec), C.byref(h)))
+        self.handle = h
+
+    def info(self):
+        v = [C.c_int64() for _ in range(4)]
+        _check(lib().padoc_tree_desc_info(self.handle, *[C.byref(x) for x in v]))
+        return {"n_tokens": v[0].value, "n_qsegs": v[1].value, "n_kvsegs": v[2].value,
+                "ancestor_pairs": v[3].value}
+
+    def segments(self):
+        inf = self.info()
+        qs = np.zeros((max(inf["n_qsegs"], 1), 4), np.int32)
+        kv = np.zeros((max(inf["n_kvsegs"], 1), 3), np.int32)
+        _check(lib().padoc_tree_desc_segments(self.handle, _p32(qs), _p32(kv)))
+        return qs[: inf["n_qsegs"]], kv[: inf["n_kvsegs"]]
+
+    def upload(self, group: int):
+        _check(lib().padoc_tree_desc_upload(self.handle, group))
+
+    def free(self):
+        if self.handle:
+            lib().padoc_tree_desc_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def tree_attn_varlen(desc: TreeDesc, q, k, v, o, lse, dtype: int, Hq: int, Hkv: int, d: int,
+                     scale: float = 0.0, stream=None):
+    _check(lib().padoc_tree_attn_varlen(desc.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), dtype, Hq,
+                                        Hkv, d, float(scale), _stream(stream)))
+
+
+# ------------------------------------------------------------------ KV pool
+
+
+class KVPool:
+    """Refcounted paged KV pool over caller-owned storage (padoc_kv_pool_*)."""
+
+    def __init__(self, k_pool, v_pool, num_blocks: int, Hkv: int, d: int = 128, max_seqs: int = 1024,
+                 max_blocks_per_seq: int = 512, block_size: int = 16, dtype: int = BF16):
+        h = C.c_void_p()
+        _check(lib().padoc_kv_pool_create(C.byref(h), _ptr(k_pool), _ptr(v_pool), num_blocks, block_size, Hkv, d,
+                                          dtype, max_seqs, max_blocks_per_seq))
+        self.handle = h
+        self.Hkv = Hkv
+        self.d = d
+        self._storage = (k_pool, v_pool)
+
+    def alloc(self, n_tokens: int = 0) -> int:
+        s = C.c_int32()
+        _check(lib().padoc_kv_alloc(self.handle, n_tokens, C.byref(s)))
+        return s.value
+
+    def fork(self, parent: int, fork_len: int) -> int:
+        s = C.c_int32()
+        _check(lib().padoc_kv_fork(self.handle, parent, fork_len, C.byref(s)))
+        return s.value
+
+    def append(self, seq: int, k, v, n: int, stream=None):
+        _check(lib().padoc_kv_append(self.handle, seq, _ptr(k), _ptr(v), n, _stream(stream)))
+
+    def release(self, seq: int):
+        _check(lib().padoc_kv_release(self.handle, seq))
+
+    def seq_info(self, seq: int):
+        a, b, c = C.c_int32(), C.c_int32(), C.c_int32()
+        _check(lib().padoc_kv_seq_info(self.handle, seq, C.byref(a), C.byref(b), C.byref(c)))
+        return {"length": a.value, "fork_len": b.value, "n_blocks": c.value}
+
+    def seq_blocks(self, seq: int):
+        n = self.seq_info(seq)["n_blocks"]
+        out = np.zeros(max(n, 1), np.int32)
+        _check(lib().padoc_kv_seq_blocks(self.handle, seq, _p32(out), len(out)))
+        return out[:n]
+
+    def refcount(self, block: int) -> int:
+        r = C.c_int32()
+        _check(lib().padoc_kv_block_refcount(self.handle, block, C.byref(r)))
+        return r.value
+
+    def stats(self):
+        a, b = C.c_int32(), C.c_int32()
+        _check(lib().padoc_kv_pool_stats(self.handle, C.byref(a), C.byref(b)))
+        return {"free_blocks": a.value, "live_seqs": b.value}
+
+    def sync(self, stream=None):
+        _check(lib().padoc_kv_pool_sync(self.handle, _stream(stream)))
+
+    def destroy(self):
+        if self.handle:
+            lib().padoc_kv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+class Batch:
+    """Host arrays of one decode/verify step (padoc_decode_batch)."""
+
+    def __init__(self, page_seq: Sequence[int], branch_offsets: Sequence[int], branch_seq: Sequence[int],
+                 q_offsets: Sequence[int]):
+        self._keep = [_i32(page_seq if len(page_seq) else [0]), _i32(branch_offsets), _i32(branch_seq or [0]),
+                      _i32(q_offsets)]
+        self.c = DecodeBatch(len(page_seq), len(branch_seq), _p32(self._keep[0]), _p32(self._keep[1]),
+                             _p32(self._keep[2]), _p32(self._keep[3]))
+        self.nq = int(self._keep[3][-1]) if len(branch_seq) else 0
+
+
+def branch_decode_ws_size(pool: KVPool, batch: Batch, Hq: int) -> int:
+    n = C.c_size_t()
+    _check(lib().padoc_branch_decode_ws_size(pool.handle, C.byref(batch.c), Hq, C.byref(n)))
+    return n.value
+
+
+def branch_decode(pool: KVPool, batch: Batch, Hq: int, q, k_new, v_new, tree_bits, o, lse, ws, ws_bytes: int,
+                  scale: float = 0.0, stream=None):
+    _check(lib().padoc_branch_decode(pool.handle, C.byref(batch.c), Hq, _ptr(q), _ptr(k_new), _ptr(v_new),
+                                     _ptr(tree_bits), _ptr(o), _ptr(lse), float(scale), _ptr(ws), int(ws_bytes),
+                                     _stream(stream)))
+
+
+# ------------------------------------------------------------------ small helpers
+
+
+def tree_mask_build(parent: Sequence[int]) -> np.ndarray:
+    p = _i32(parent if len(parent) else [0])
+    out = np.zeros(max(len(parent), 1), np.uint16)
+    _check(lib().padoc_tree_mask_build(_p32(p), len(parent), out.ctypes.data_as(C.POINTER(C.c_uint16))))
+    return out[: len(parent)]
+
+
+def depths(layout_len: Sequence[int], content_len: Sequence[int]):
+    a, b = _i32(list(layout_len) or [0]), _i32(list(content_len) or [0])
+    s, t = C.c_int64(), C.c_int64()
+    _check(lib().padoc_depths(_p32(a), _p32(b), len(layout_len), C.byref(s), C.byref(t)))
+    return {"D_seq": s.value, "D_tree": t.value}
+
+
+def device_status(stream=None):
+    _check(lib().padoc_device_status(_stream(stream)))
