@@ -1,0 +1,397 @@
+#!/usr/bin/env python3
+"""Benchmark of ancestor-masked tree attention over a shared page-prefix KV
+cache on one or more GPUs (one process per GPU, weak scaling).
+
+A step runs both regimes of the hot path on the serving-scale workload:
+  * branch decode: 512 pages, prefix U[4000, 6144] tokens, 8-60 branches per
+    page (zero-copy forks of the page prefix), own suffix U[0, 1024], one
+    query token per live branch (about 17.6 k branches); kernels: the cascade
+    prefix pass and the own-suffix pass with the log-sum-exp merge;
+  * tree-varlen forward: 8 packed sequences of 16384 tokens built from the
+    same page-length distributions.
+`value` is branch-decode attention tokens per second (query tokens of all
+ranks divided by the slowest rank's decode time); the forward's TFLOP/s and
+both roofline fractions ride along in the same JSON line.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "branch-decode attn tokens/s & % HBM roofline; tree-varlen fwd TFLOP/s & % peak"
+WORKLOAD = ("serving-scale: branch decode over 512 pages (prefix U[4000,6144], 8-60 branches/page, "
+            "own suffix U[0,1024], 1 query/branch) + tree-varlen forward over 8 x 16384 packed tokens; "
+            "bf16, Hq=16, Hkv=8, d=128")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "of measured"
+    return FALLBACK_PEAKS, "of fallback"
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+
+def _oracle_decode_pages(args):
+    """Child process: the oracle's branch decode over sampled pages, timed."""
+    seed, page_ids = args
+    sys.path.insert(0, ROOT)
+    from oracle import tree_attention as ta
+    from tree_structured_shared_gb300 import workloads as wl
+    full = wl.serving_decode(seed)
+    sub = wl.DecodeWorkload("sample", [full.pages[i] for i in page_ids], full.Hq, full.Hkv, full.d,
+                            full.value_scale)
+    vals = wl.decode_values(sub, seed + 17)
+    t0 = time.perf_counter()
+    ta.branch_decode(sub, vals, tree=False)
+    return time.perf_counter() - t0, sub.n_queries
+
+
+def _oracle_forward_rows(args):
+    """Child process: the oracle's forward on sampled rows of one packed page."""
+    seed, n_rows = args
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    from oracle import tree_attention as ta
+    from tree_structured_shared_gb300 import workloads as wl
+    full = wl.packed_sequences(seed)
+    page = wl.TreeWorkload("p", [full.pages[0]], full.Hq, full.Hkv, full.d, "bf16", 0.5, [0])
+    q, k, v = wl.tree_qkv(page, seed)
+    rng = np.random.default_rng(seed)
+    rows = sorted(rng.choice(page.n_tokens, n_rows, replace=False).tolist())
+    anc = ta.ancestor_positions(page.pages)
+    pairs = sum(len(anc[r]) for r in rows)
+    t0 = time.perf_counter()
+    ta.tree_forward(q, k, v, page.pages, positions=rows)
+    return time.perf_counter() - t0, 4.0 * page.d * page.Hq * pairs
+
+
+def cpu_oracle_baseline(seed: int, n_pages: int, fwd_rows: int):
+    """The oracle as it stands, on the host cores, over a bounded sample."""
+    cores = len(os.sched_getaffinity(0))
+    used = min(cores, n_pages)
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(processes=used) as pool:
+        res = pool.map(_oracle_decode_pages, [(seed, [i]) for i in range(n_pages)])
+        nf = min(used, 4)
+        fwd = pool.map(_oracle_forward_rows, [(seed + i, fwd_rows) for i in range(nf)])
+    wall = time.perf_counter() - t0
+    dec_tokens = sum(r[1] for r in res)
+    dec_cpu = sum(r[0] for r in res)
+    fwd_cpu = sum(r[0] for r in fwd)
+    return {
+        "value": dec_tokens / (dec_cpu / used),
+        "unit": "tokens/s",
+        "cores": used,
+        "kind": "oracle",
+        "sample": (f"{n_pages} of the 512 decode pages ({dec_tokens} branch queries), one page per process, "
+                   f"float64 NumPy; rate = queries / (summed oracle seconds / processes); forward: {fwd_rows} "
+                   f"sampled query rows of one packed page in each of {nf} processes"),
+        "cpu_seconds": round(dec_cpu + fwd_cpu, 2),
+        "wall_seconds": round(wall, 2),
+        "forward_tflops": sum(r[1] for r in fwd) / (fwd_cpu / nf) / 1e12,
+    }
+
+
+def run_reference(args, rank: int) -> int:
+    """Reference arm: the float64 oracle on host cores, same metric."""
+    if rank != 0:
+        return 0
+    cores = len(os.sched_getaffinity(0))
+    per_step = max(1, min(cores, 4))
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(processes=per_step) as pool:
+        for w in range(args.warmup):
+            pool.map(_oracle_decode_pages, [(args.seed, [w % 512])])
+        toks = 0
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            ids = [(s * per_step + i) % 512 for i in range(per_step)]
+            res = pool.map(_oracle_decode_pages, [(args.seed, [i]) for i in ids])
+            toks += sum(r[1] for r in res)
+        total = time.perf_counter() - t0
+    value = toks / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "reference": "float64 CPU oracle (the pages publish no implementation)",
+                   "per_step": f"{per_step} decode pages, one per process"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": per_step, "kind": "oracle",
+                         "sample": f"{per_step} pages of the 512-page decode workload per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="padoc_clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx = float(p[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def traffic_for(kernel: str, units: float):
+    """DRAM bytes per launch from the committed ncu summary, scaled by units,
+    or None when the kernel's source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "tree_structured_shared_gb300", "csrc", d["source"])
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha"]:
+        return None
+    return d["dram_bytes"] / d["units"] * units
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-pages", type=int, default=32, help="decode pages in the CPU oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps")
+
+    # the CPU baseline's process pool runs before any CUDA work (spawn)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_baseline(args.seed, args.cpu_pages, 64)
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    from tree_structured_shared_gb300 import build, harness, padoc
+    from tree_structured_shared_gb300 import workloads as wl
+    if not os.path.exists(padoc.LIB_PATH):
+        build.build()
+    seed = args.seed + 1000 * rank  # independent pages per rank
+
+    dw = wl.serving_decode(seed)
+    fw = wl.packed_sequences(seed)
+    dec = harness.Decode(dw, seed=seed, tree=False)
+    fwd = harness.Forward(fw, seed=seed)
+    dec.plan()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        dec.prefix_pass()
+        dec.own_pass()
+        fwd.run()
+    torch.cuda.synchronize()
+    padoc.device_status()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for s in range(K):
+        ev[s][0].record(stream)
+        dec.prefix_pass()
+        ev[s][1].record(stream)
+        dec.own_pass()
+        ev[s][2].record(stream)
+        fwd.run()
+        ev[s][3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    padoc.device_status()
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    t_own = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    t_fwd = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    t_dec = t_pre + t_own
+    times = torch.tensor([t_dec, t_fwd, t_pre, t_own], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    t_dec, t_fwd, t_pre, t_own = [float(x) for x in times.tolist()]
+
+    # end to end through the all-in-one C-ABI call, inputs from pinned host memory
+    e2e = None
+    nq = dec.nq
+    if not args.no_e2e:
+        h_q = torch.empty(dec.q.shape, dtype=dec.q.dtype, pin_memory=True)
+        h_k = torch.empty(dec.k_new.shape, dtype=dec.k_new.dtype, pin_memory=True)
+        h_v = torch.empty(dec.v_new.shape, dtype=dec.v_new.dtype, pin_memory=True)
+        h_q.copy_(dec.q)
+        h_k.copy_(dec.k_new)
+        h_v.copy_(dec.v_new)
+        h_o = torch.empty(dec.o.shape, dtype=dec.o.dtype, pin_memory=True)
+        h_l = torch.empty(dec.lse.shape, dtype=dec.lse.dtype, pin_memory=True)
+        d_q, d_k, d_v = torch.empty_like(dec.q), torch.empty_like(dec.k_new), torch.empty_like(dec.v_new)
+
+        def e2e_step():
+            d_q.copy_(h_q, non_blocking=True)
+            d_k.copy_(h_k, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            padoc.branch_decode(dec.pool, dec.batch, dw.Hq, d_q, d_k, d_v, None, dec.o, dec.lse, dec.ws,
+                                dec.ws_bytes)
+            h_o.copy_(dec.o, non_blocking=True)
+            h_l.copy_(dec.lse, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        torch.cuda.synchronize()
+        te = torch.tensor([(time.perf_counter() - t0) / K], dtype=torch.float64, device="cuda")
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        te = float(te.item())
+        e2e = {"value": nq * world / te, "unit": "tokens/s",
+               "h2d_bytes_per_step": (h_q.numel() + h_k.numel() + h_v.numel()) * 2,
+               "d2h_bytes_per_step": h_o.numel() * 2 + h_l.numel() * 4, "ms_per_step": te * 1000,
+               "includes": "host plan build, block-table and plan upload, both passes, input and output copies"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tf_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    own_b, pre_b, all_b = dec.own_bytes(), dec.prefix_bytes(), dec.unique_kv_bytes()
+    fl = fwd.flops
+    own_gbs = own_b / (t_own * 1e-3) / 1e9
+    pre_gbs = pre_b / (t_pre * 1e-3) / 1e9
+    dec_gbs = all_b / (t_dec * 1e-3) / 1e9
+    fwd_tf = fl / (t_fwd * 1e-3) / 1e12
+    own_units = sum(sum(p.own_len) for p in dw.pages)
+    line = {
+        "metric": METRIC,
+        "value": nq * world / (t_dec * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": t_dec,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "pages": len(dw.pages), "branches": dw.n_branches, "query_tokens": nq,
+                   "forward_tokens": fw.n_tokens,
+                   "l2": "inputs larger than L2 (decode KV about 48 GB, forward Q/K/V 1.3 GB)",
+                   "step": ("value and ms_per_step cover the decode step (prefix pass + own pass); the forward "
+                            "runs in the same timed loop and is reported under 'forward'"),
+                   "parallelism": f"dp{world} (independent pages per GPU)"},
+        "roofline": {"bound": "hbm", "kernel": "own_pass_kernel", "achieved": own_gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": own_gbs / hbm, "peak_source": peak_src,
+                     "traffic": traffic_for("own_pass", own_units), "algorithmic_bytes": own_b, "ms": t_own},
+        "kernels": {
+            "prefix_pass": {"ms": t_pre, "achieved_gbs": pre_gbs, "frac_hbm": pre_gbs / hbm,
+                            "algorithmic_bytes": pre_b},
+            "own_pass": {"ms": t_own, "achieved_gbs": own_gbs, "frac_hbm": own_gbs / hbm,
+                         "algorithmic_bytes": own_b},
+            "decode_step": {"ms": t_dec, "achieved_gbs": dec_gbs, "frac_hbm": dec_gbs / hbm,
+                            "frac_spec_8tbs": dec_gbs / 8000.0, "algorithmic_bytes": all_b},
+        },
+        "forward": {"ms": t_fwd, "tflops": fwd_tf * world, "tflops_per_gpu": fwd_tf, "bound": "tensor",
+                    "peak": tf_sus, "peak_kind": "bf16 sustained " + peak_src, "frac": fwd_tf / tf_sus,
+                    "frac_spec_2250": fwd_tf / 2250.0, "algorithmic_flops": fl,
+                    "traffic": traffic_for("forward", fw.n_tokens)},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -221,6 +221,37 @@ PADOC_API int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch*
                         const uint16_t* tree_bits, void* o, float* lse, float scale, void* ws,
                         size_t ws_bytes, padoc_stream_t stream);
 
+/* ---- The same step split into a plan and its two device passes. ----
+ * A plan is host state built from the pool and the batch.  It stays valid
+ * until the pool changes (alloc/append/fork/release); build the next step's
+ * plan while the current one runs.
+ *   padoc_decode_plan_create  validates and plans (host only)
+ *   padoc_decode_plan_ws_size workspace bytes the plan needs
+ *   padoc_decode_plan_upload  uploads changed block-table rows and copies the
+ *                             plan into ws (enqueued on stream)
+ *   padoc_decode_prefix_pass  kernel 1: per page, kv head and prefix chunk,
+ *                             the partial softmax of every query row of the
+ *                             page over the chunk's shared blocks (tensor
+ *                             cores; each prefix block read once per page)
+ *   padoc_decode_own_pass     kernel 2: per branch and kv head, the own
+ *                             suffix and the query block under the tree mask,
+ *                             then the log-sum-exp merge with kernel 1's
+ *                             partials into o and lse
+ * Arguments mean what they mean for padoc_branch_decode; ws must hold the
+ * uploaded plan.  The own pass reads what the prefix pass wrote to ws, so
+ * run them in this order on one stream. */
+typedef struct padoc_decode_plan padoc_decode_plan;
+PADOC_API int padoc_decode_plan_create(padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq,
+                                       padoc_decode_plan** out);
+PADOC_API int padoc_decode_plan_ws_size(const padoc_decode_plan* plan, size_t* bytes);
+PADOC_API int padoc_decode_plan_upload(padoc_decode_plan* plan, void* ws, size_t ws_bytes, padoc_stream_t stream);
+PADOC_API int padoc_decode_prefix_pass(const padoc_decode_plan* plan, const void* q, float scale, void* ws,
+                                       padoc_stream_t stream);
+PADOC_API int padoc_decode_own_pass(const padoc_decode_plan* plan, const void* q, const void* k_new,
+                                    const void* v_new, const uint16_t* tree_bits, void* o, float* lse,
+                                    float scale, void* ws, padoc_stream_t stream);
+PADOC_API int padoc_decode_plan_free(padoc_decode_plan* plan);
+
 /* Draft-tree visibility (HSD page, "prefix-tree batching"): for n <= 16 nodes
  * in topological order (parent[i] < i, -1 for a root), bits[i] gets bit j set
  * iff node j is node i or one of its ancestors.  Host arrays. */

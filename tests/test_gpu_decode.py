@@ -114,3 +114,18 @@ def test_decode_rejects_bad_batches(harness):
     with pytest.raises(padoc.PadocError):
         padoc.branch_decode(d.pool, d.batch, w.Hq, d.q, d.k_new, d.v_new, None, d.o, d.lse, d.ws, 16)
     torch.cuda.synchronize()
+
+
+def test_plan_and_passes_equal_all_in_one(harness):
+    """The planned two-pass path writes the same bits as padoc_branch_decode."""
+    import torch
+    w = wl.small_decode(31, n_pages=3, max_prefix=500, max_branches=5, max_own=200, Hq=4, Hkv=2)
+    d = harness.Decode(w, wl.decode_values(w, 31), tree=True)
+    o1, l1 = [x.clone() for x in d.run()]
+    d.o.zero_()
+    d.lse.zero_()
+    d.plan()
+    d.prefix_pass()
+    d.own_pass()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, d.o) and torch.equal(l1, d.lse)

@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <memory>
@@ -837,32 +838,76 @@ extern "C" int padoc_branch_decode_ws_size(const padoc_kv_pool* pool, const pado
   return PADOC_OK;
 }
 
-extern "C" int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq, const void* q,
-                                   const void* k_new, const void* v_new, const uint16_t* tree_bits, void* o,
-                                   float* lse, float scale, void* ws, size_t ws_bytes, padoc_stream_t stream) {
+struct padoc_decode_plan {
+  padoc_kv_pool* pool = nullptr;
+  int32_t Hq = 0;
+  int32_t n_pages = 0, n_branches = 0;
   DecodePlan pl;
-  int rc;
-  PADOC_TRY(rc = plan_decode(pool, batch, Hq, num_sms(), &pl));
+  std::vector<uint8_t> host;  // plan arrays as they are laid out in ws
+};
+
+extern "C" int padoc_decode_plan_create(padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq,
+                                        padoc_decode_plan** out) {
+  if (!out) return fail(PADOC_ERR_INVALID, "decode_plan_create: null out");
+  *out = nullptr;
+  padoc_decode_plan* res = nullptr;
+  PADOC_TRY({
+    std::unique_ptr<padoc_decode_plan> p(new padoc_decode_plan());
+    const int rc = plan_decode(pool, batch, Hq, num_sms(), &p->pl);
+    if (rc) return rc;
+    p->pool = pool;
+    p->Hq = Hq;
+    p->n_pages = batch->n_pages;
+    p->n_branches = batch->n_branches;
+    p->host.assign(p->pl.off_part_o, 0);
+    std::memcpy(p->host.data() + p->pl.off_pages, p->pl.pages.data(), p->pl.pages.size() * sizeof(DecPage));
+    std::memcpy(p->host.data() + p->pl.off_items, p->pl.items.data(), p->pl.items.size() * sizeof(DecItem));
+    std::memcpy(p->host.data() + p->pl.off_branches, p->pl.branches.data(),
+                p->pl.branches.size() * sizeof(DecBranch));
+    std::memcpy(p->host.data() + p->pl.off_qplen, p->pl.q_plen.data(), p->pl.q_plen.size() * sizeof(int32_t));
+    res = p.release();
+  });
+  *out = res;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_decode_plan_free(padoc_decode_plan* plan) {
+  delete plan;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_decode_plan_ws_size(const padoc_decode_plan* plan, size_t* bytes) {
+  if (!plan || !bytes) return fail(PADOC_ERR_INVALID, "decode_plan_ws_size: null argument");
+  *bytes = plan->pl.total;
+  return PADOC_OK;
+}
+
+static int check_ws(const padoc_decode_plan* plan, const void* ws, size_t ws_bytes) {
+  if (!ws) return fail(PADOC_ERR_INVALID, "decode: null workspace");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(PADOC_ERR_INVALID, "decode: ws must be 256-byte aligned");
+  if (ws_bytes < plan->pl.total)
+    return fail(PADOC_ERR_INVALID, "decode: workspace %zu bytes, need %zu", ws_bytes, plan->pl.total);
+  return PADOC_OK;
+}
+
+extern "C" int padoc_decode_plan_upload(padoc_decode_plan* plan, void* ws, size_t ws_bytes, padoc_stream_t stream) {
+  if (!plan) return fail(PADOC_ERR_INVALID, "decode_plan_upload: null plan");
+  if (plan->n_branches == 0) return PADOC_OK;
+  int rc = check_ws(plan, ws, ws_bytes);
   if (rc) return rc;
-  if (batch->n_branches == 0) return PADOC_OK;
-  if (!q || !k_new || !v_new || !o || !lse || !ws) return fail(PADOC_ERR_INVALID, "branch_decode: null tensor");
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(o) || !aligned16(lse))
-    return fail(PADOC_ERR_INVALID, "branch_decode: tensors must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(PADOC_ERR_INVALID, "branch_decode: ws must be 256-byte aligned");
-  if (ws_bytes < pl.total) return fail(PADOC_ERR_INVALID, "branch_decode: workspace %zu bytes, need %zu", ws_bytes, pl.total);
-  if (!pool->k || !pool->v) return fail(PADOC_ERR_INVALID, "branch_decode: pool has no storage");
+  if (!plan->pool->k || !plan->pool->v) return fail(PADOC_ERR_INVALID, "decode: pool has no storage");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  rc = pool_sync(pool, st);
+  rc = pool_sync(plan->pool, st);
   if (rc) return rc;
-  // one host buffer holding the plan arrays, copied in one transfer
-  std::vector<uint8_t> host;
-  PADOC_TRY(host.assign(pl.off_part_o, 0));
-  std::memcpy(host.data() + pl.off_pages, pl.pages.data(), pl.pages.size() * sizeof(DecPage));
-  std::memcpy(host.data() + pl.off_items, pl.items.data(), pl.items.size() * sizeof(DecItem));
-  std::memcpy(host.data() + pl.off_branches, pl.branches.data(), pl.branches.size() * sizeof(DecBranch));
-  std::memcpy(host.data() + pl.off_qplen, pl.q_plen.data(), pl.q_plen.size() * sizeof(int32_t));
-  cudaError_t e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return cuda_fail(e, "branch_decode: plan upload");
+  cudaError_t e = cudaMemcpyAsync(ws, plan->host.data(), plan->host.size(), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode: plan upload");
+  return PADOC_OK;
+}
+
+static DecodeArgs decode_args(const padoc_decode_plan* plan, const void* q, const void* k_new, const void* v_new,
+                              const uint16_t* tree_bits, void* o, float* lse, float scale, void* ws) {
+  const DecodePlan& pl = plan->pl;
+  const padoc_kv_pool* pool = plan->pool;
   uint8_t* w = static_cast<uint8_t*>(ws);
   DecodeArgs a;
   a.pages = reinterpret_cast<const DecPage*>(w + pl.off_pages);
@@ -871,13 +916,13 @@ extern "C" int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch
   a.q_plen = reinterpret_cast<const int32_t*>(w + pl.off_qplen);
   a.table = pool->d_table;
   a.max_bps = pool->max_bps;
-  a.n_pages = batch->n_pages;
+  a.n_pages = plan->n_pages;
   a.n_items = static_cast<int32_t>(pl.items.size());
-  a.n_branches = batch->n_branches;
+  a.n_branches = plan->n_branches;
   a.nq = static_cast<int32_t>(pl.q_plen.size());
-  a.Hq = Hq;
+  a.Hq = plan->Hq;
   a.Hkv = pool->Hkv;
-  a.group = Hq / pool->Hkv;
+  a.group = plan->Hq / pool->Hkv;
   a.d = pool->d;
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(pool->d));
   a.q = q;
@@ -891,14 +936,56 @@ extern "C" int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch
   a.k_pool = pool->k;
   a.v_pool = pool->v;
   a.num_blocks = pool->nb;
+  return a;
+}
+
+extern "C" int padoc_decode_prefix_pass(const padoc_decode_plan* plan, const void* q, float scale, void* ws,
+                                        padoc_stream_t stream) {
+  if (!plan) return fail(PADOC_ERR_INVALID, "decode_prefix_pass: null plan");
+  if (plan->n_branches == 0 || plan->pl.items.empty()) return PADOC_OK;
+  int rc = check_ws(plan, ws, SIZE_MAX);
+  if (rc) return rc;
+  if (!q || !aligned16(q)) return fail(PADOC_ERR_INVALID, "decode_prefix_pass: q must be a 16-byte aligned device pointer");
+  if (!plan->pool->d_table) return fail(PADOC_ERR_INVALID, "decode_prefix_pass: plan was not uploaded");
+  const DecodeArgs a = decode_args(plan, q, nullptr, nullptr, nullptr, nullptr, nullptr, scale, ws);
   std::string err;
-  if (a.n_items > 0) {
-    rc = launch_decode_prefix(a, st, &err);
-    if (rc) return fail(rc, "branch_decode: %s", err.c_str());
-  }
-  rc = launch_decode_own(a, st, &err);
-  if (rc) return fail(rc, "branch_decode: %s", err.c_str());
+  rc = launch_decode_prefix(a, reinterpret_cast<cudaStream_t>(stream), &err);
+  if (rc) return fail(rc, "decode_prefix_pass: %s", err.c_str());
   return PADOC_OK;
+}
+
+extern "C" int padoc_decode_own_pass(const padoc_decode_plan* plan, const void* q, const void* k_new,
+                                     const void* v_new, const uint16_t* tree_bits, void* o, float* lse, float scale,
+                                     void* ws, padoc_stream_t stream) {
+  if (!plan) return fail(PADOC_ERR_INVALID, "decode_own_pass: null plan");
+  if (plan->n_branches == 0) return PADOC_OK;
+  int rc = check_ws(plan, ws, SIZE_MAX);
+  if (rc) return rc;
+  if (!q || !k_new || !v_new || !o || !lse) return fail(PADOC_ERR_INVALID, "decode_own_pass: null tensor");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(o) || !aligned16(lse))
+    return fail(PADOC_ERR_INVALID, "decode_own_pass: tensors must be 16-byte aligned");
+  if (!plan->pool->d_table) return fail(PADOC_ERR_INVALID, "decode_own_pass: plan was not uploaded");
+  const DecodeArgs a = decode_args(plan, q, k_new, v_new, tree_bits, o, lse, scale, ws);
+  std::string err;
+  rc = launch_decode_own(a, reinterpret_cast<cudaStream_t>(stream), &err);
+  if (rc) return fail(rc, "decode_own_pass: %s", err.c_str());
+  return PADOC_OK;
+}
+
+extern "C" int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq, const void* q,
+                                   const void* k_new, const void* v_new, const uint16_t* tree_bits, void* o,
+                                   float* lse, float scale, void* ws, size_t ws_bytes, padoc_stream_t stream) {
+  padoc_decode_plan* plan = nullptr;
+  int rc = padoc_decode_plan_create(pool, batch, Hq, &plan);
+  if (rc) return rc;
+  std::unique_ptr<padoc_decode_plan> guard(plan);
+  if (plan->n_branches == 0) return PADOC_OK;
+  if (!q || !k_new || !v_new || !o || !lse) return fail(PADOC_ERR_INVALID, "branch_decode: null tensor");
+  rc = padoc_decode_plan_upload(plan, ws, ws_bytes, stream);
+  if (rc) return rc;
+  rc = padoc_decode_prefix_pass(plan, q, scale, ws, stream);
+  if (rc) return rc;
+  return padoc_decode_own_pass(plan, q, k_new, v_new, tree_bits, o, lse, scale, ws, stream);
 }
 
 // ============================================================== small host helpers

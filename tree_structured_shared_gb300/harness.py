@@ -161,6 +161,33 @@ class Decode:
                             self.o, self.lse, self.ws, self.ws_bytes, 0.0, stream)
         return self.o, self.lse
 
+    def plan(self):
+        """Plans the step and uploads the plan into ws (before a timed region)."""
+        self._plan = padoc.DecodePlan(self.pool, self.batch, self.w.Hq)
+        self._plan.upload(self.ws, self.ws_bytes)
+        return self._plan
+
+    def prefix_pass(self, stream=None):
+        self._plan.prefix_pass(self.q, self.ws, 0.0, stream)
+
+    def own_pass(self, stream=None):
+        self._plan.own_pass(self.q, self.k_new, self.v_new, self.tree_bits, self.o, self.lse, self.ws, 0.0, stream)
+
+    def prefix_bytes(self) -> int:
+        """Algorithmic bytes of the prefix pass: each page's shared prefix
+        tokens once (K and V, all kv heads) and the query rows."""
+        w = self.w
+        row = w.Hkv * w.d * 2 * 2
+        return sum(max(p.branch_prefix_len or [0]) for p in w.pages) * row + self.nq * w.Hq * w.d * 2
+
+    def own_bytes(self) -> int:
+        """Algorithmic bytes of the own pass: each own cached token once, the
+        query block's Q, K and V, O and LSE out."""
+        w = self.w
+        row = w.Hkv * w.d * 2 * 2
+        return (sum(sum(p.own_len) for p in w.pages) * row + self.nq * row + self.nq * w.Hq * w.d * 2 * 2
+                + self.nq * w.Hq * 4)
+
     def unique_kv_bytes(self) -> int:
         """Algorithmic bytes of one step: each shared prefix token once per
         page (the longest prefix any of its branches sees), each own token

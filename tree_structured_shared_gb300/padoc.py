@@ -27,7 +27,8 @@ EXPORTED = [
     "padoc_kv_append", "padoc_kv_fork", "padoc_kv_release", "padoc_kv_seq_info", "padoc_kv_seq_blocks",
     "padoc_kv_block_refcount", "padoc_kv_pool_stats", "padoc_kv_pool_sync",
     "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
-    "padoc_device_status",
+    "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_upload",
+    "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free",
 ]
 
 
@@ -87,6 +88,12 @@ def lib() -> C.CDLL:
             "padoc_tree_mask_build": (C.c_int, [p32, i32, C.POINTER(C.c_uint16)]),
             "padoc_depths": (C.c_int, [p32, p32, i32, p64, p64]),
             "padoc_device_status": (C.c_int, [vp]),
+            "padoc_decode_plan_create": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, C.POINTER(vp)]),
+            "padoc_decode_plan_ws_size": (C.c_int, [vp, C.POINTER(C.c_size_t)]),
+            "padoc_decode_plan_upload": (C.c_int, [vp, vp, C.c_size_t, vp]),
+            "padoc_decode_prefix_pass": (C.c_int, [vp, vp, f32, vp, vp]),
+            "padoc_decode_own_pass": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp]),
+            "padoc_decode_plan_free": (C.c_int, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -275,6 +282,43 @@ def branch_decode(pool: KVPool, batch: Batch, Hq: int, q, k_new, v_new, tree_bit
     _check(lib().padoc_branch_decode(pool.handle, C.byref(batch.c), Hq, _ptr(q), _ptr(k_new), _ptr(v_new),
                                      _ptr(tree_bits), _ptr(o), _ptr(lse), float(scale), _ptr(ws), int(ws_bytes),
                                      _stream(stream)))
+
+
+class DecodePlan:
+    """A planned decode step (padoc_decode_plan_*): host plan, upload, and the
+    two device passes."""
+
+    def __init__(self, pool: KVPool, batch: Batch, Hq: int):
+        h = C.c_void_p()
+        _check(lib().padoc_decode_plan_create(pool.handle, C.byref(batch.c), Hq, C.byref(h)))
+        self.handle = h
+        self._refs = (pool, batch)
+
+    def ws_size(self) -> int:
+        n = C.c_size_t()
+        _check(lib().padoc_decode_plan_ws_size(self.handle, C.byref(n)))
+        return n.value
+
+    def upload(self, ws, ws_bytes: int, stream=None):
+        _check(lib().padoc_decode_plan_upload(self.handle, _ptr(ws), int(ws_bytes), _stream(stream)))
+
+    def prefix_pass(self, q, ws, scale: float = 0.0, stream=None):
+        _check(lib().padoc_decode_prefix_pass(self.handle, _ptr(q), float(scale), _ptr(ws), _stream(stream)))
+
+    def own_pass(self, q, k_new, v_new, tree_bits, o, lse, ws, scale: float = 0.0, stream=None):
+        _check(lib().padoc_decode_own_pass(self.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(tree_bits),
+                                           _ptr(o), _ptr(lse), float(scale), _ptr(ws), _stream(stream)))
+
+    def free(self):
+        if self.handle:
+            lib().padoc_decode_plan_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
 
 
 # ------------------------------------------------------------------ small helpers
