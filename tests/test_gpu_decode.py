@@ -129,3 +129,20 @@ def test_plan_and_passes_equal_all_in_one(harness):
     d.own_pass()
     torch.cuda.synchronize()
     assert torch.equal(o1, d.o) and torch.equal(l1, d.lse)
+
+
+def test_repeat_decode_bit_identical(harness):
+    import torch
+    w = wl.spec_verify(1)
+    w.pages = w.pages[:12]
+    d = harness.Decode(w, seed=1, tree=True)
+    d.plan()
+    d.prefix_pass()
+    d.own_pass()
+    o0, l0 = d.o.clone(), d.lse.clone()
+    for _ in range(4):
+        d.prefix_pass()
+        d.own_pass()
+        torch.cuda.synchronize()
+        assert torch.equal(d.o, o0) and torch.equal(d.lse, l0)
+    padoc.device_status()

@@ -104,3 +104,17 @@ def test_unsupported_shapes_rejected(harness):
     w = wl.TreeWorkload("x", [wl.Page(8, [], [])], 6, 2, 128, "bf16", 1.0, [0])  # group 3
     with pytest.raises(padoc.PadocError):
         harness.Forward(w)
+
+
+def test_repeat_runs_bit_identical(harness):
+    """Many units of many key tiles, run repeatedly: any ordering race in the
+    pipeline shows up as a difference between runs."""
+    import torch
+    w = wl.packed_sequences(3, n_seq=1, seq_tokens=16384)
+    f = harness.Forward(w, seed=3)
+    o0, l0 = [x.clone() for x in f.run()]
+    for _ in range(4):
+        o, l = f.run()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    padoc.device_status()

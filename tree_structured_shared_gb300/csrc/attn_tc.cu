@@ -69,7 +69,7 @@ enum {
   B_S_FULL = 10,  // +buffer
   B_S_FREE = 12,
   B_P_FULL = 14,
-  B_P_EMPTY = 16,
+  B_SPARE = 16,  // two unused slots
   B_O_DONE = 18,
   B_O_FREE = 19,
   N_BARS = 20
@@ -387,7 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss(t_o, sdesc_sw128(pa + aoff, 16, 1024), sdesc_sw128(va + kk * 2048, kHalf, 1024), id_pv,
                         (j > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(B_P_EMPTY + pb));
           mma_commit(bar(B_V_EMPTY + st));
           mma_commit(bar(B_O_DONE));
           ++v_it;
@@ -465,24 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 1; c < 128; ++c) tmax = fmaxf(tmax, s[c]);
         const float mt = tmax * p.sl2;
         const bool grow = mt > m_run + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, grow) && j > 0) {
-          // O holds sums with the old max: rescale it before the next P V lands
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (pv_base + j - 1) & 1, abort))) { failed = true; break; }
-          tc_fence_after();
-          const float alpha = grow ? fast_exp2(m_run - mt) : 1.f;
-          uint32_t v[32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tmem + 256 + lane_base + c * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(tmem + 256 + lane_base + c * 32, v);
-          }
-          tmem_wait_st();
-        }
+        const float alpha = grow ? fast_exp2(m_run - mt) : 1.f;  // 0 while m_run is -inf
         if (grow) {
-          l_run *= fast_exp2(m_run - mt);
+          l_run *= alpha;
           m_run = mt;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
@@ -493,8 +477,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           lsum += s[c];
         }
         l_run += lsum;
+        // Every P V product completes one O_DONE phase; wait for each one in
+        // order (a parity wait is only sound one phase behind).  Once P V of
+        // tile j-1 is done, O is stable and both P buffers are free.
+        if (j > 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (pv_base + j - 1) & 1, abort))) { failed = true; break; }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, grow)) {
+            // O holds sums taken against the old max: rescale before P V of tile j
+            uint32_t v[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              tmem_ld32(tmem + 256 + lane_base + c * 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st32(tmem + 256 + lane_base + c * 32, v);
+            }
+            tmem_wait_st();
+          }
+        }
         const int pb = p_it & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_P_EMPTY + pb), ((p_it >> 1) & 1) ^ 1, abort))) { failed = true; break; }
         const uint32_t pa = sbase + SM_P + pb * 2 * kHalf;
 #pragma unroll
         for (int c = 0; c < 16; ++c)
