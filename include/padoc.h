@@ -262,6 +262,41 @@ PADOC_API int padoc_tree_mask_build(const int32_t* parent, int32_t n, uint16_t* 
 PADOC_API int padoc_depths(const int32_t* layout_len, const int32_t* content_len, int32_t n_regions,
                  int64_t* d_seq, int64_t* d_tree);
 
+/* ------------------------------------------------------------------------
+ * Branch decode without any device allocation.  (The papers have no
+ * counterpart: this serves embedding, not the method.)
+ *
+ * Some callers may not call cudaMalloc at all: a host runtime that hands the
+ * whole GPU to its own memory arena and owns every byte, a plug-in that lives
+ * inside such a runtime, or a latency-critical loop that cannot afford the
+ * device-wide synchronisation an allocation can cause.  They cannot provide
+ * the workspace padoc_branch_decode needs.  This entry point computes the
+ * same step with the workspace taken from one fixed array that the library
+ * places in device memory when it is loaded (PADOC_NOALLOC_SCRATCH_BYTES on
+ * every GPU that loads the library, held until the process exits).
+ *
+ * Arguments are those of padoc_branch_decode without ws / ws_bytes.
+ *  - A step whose workspace (padoc_branch_decode_ws_size) exceeds
+ *    PADOC_NOALLOC_SCRATCH_BYTES is rejected with PADOC_ERR_INVALID before
+ *    any device work.  As a guide, a 16-page step with one query per branch
+ *    needs about 10 MiB.
+ *  - The pool's device block table must already exist (call
+ *    padoc_kv_pool_sync once at set-up); otherwise PADOC_ERR_INVALID.
+ *  - No device memory is allocated or freed; the host plan lives on the host
+ *    heap.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero: each call writes every byte it
+ *    later reads.  Calls whose work overlaps on the GPU (other streams, other
+ *    host threads) race on the array; order them on one stream. */
+#define PADOC_NOALLOC_SCRATCH_BYTES (32u << 20)
+PADOC_API int padoc_branch_decode_noalloc(padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq,
+                                          const void* q, const void* k_new, const void* v_new,
+                                          const uint16_t* tree_bits, void* o, float* lse, float scale,
+                                          padoc_stream_t stream);
+
 /* Reports and clears the device error word of the current device: 0 when no
  * kernel has given up a wait since the last call, else PADOC_ERR_DEVICE_TIMEOUT
  * with the failing site in the message. */

@@ -988,6 +988,11 @@ extern "C" int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch
   return padoc_decode_own_pass(plan, q, k_new, v_new, tree_bits, o, lse, scale, ws, stream);
 }
 
+namespace padoc {
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+bool pool_has_device_table(const padoc_kv_pool* pool) { return pool && pool->d_table; }
+}  // namespace padoc
+
 // ============================================================== small host helpers
 
 extern "C" int padoc_tree_mask_build(const int32_t* parent, int32_t n, uint16_t* bits) {

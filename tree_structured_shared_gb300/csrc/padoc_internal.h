@@ -117,4 +117,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 EncodeTiledFn get_encode_fn(std::string* err);
 int num_sms();
 
+// Records an error message for padoc_last_error() and returns code.
+int set_error(int code, const char* msg);
+// True once the pool's device block table exists (padoc_kv_pool_sync ran).
+bool pool_has_device_table(const padoc_kv_pool* pool);
+
 }  // namespace padoc

@@ -28,8 +28,9 @@ EXPORTED = [
     "padoc_kv_block_refcount", "padoc_kv_pool_stats", "padoc_kv_pool_sync",
     "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
     "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_upload",
-    "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free",
+    "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free", "padoc_branch_decode_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class PadocError(RuntimeError):
@@ -94,6 +95,8 @@ def lib() -> C.CDLL:
             "padoc_decode_prefix_pass": (C.c_int, [vp, vp, f32, vp, vp]),
             "padoc_decode_own_pass": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp]),
             "padoc_decode_plan_free": (C.c_int, [vp]),
+            "padoc_branch_decode_noalloc": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, vp, vp, vp, vp, vp, vp, f32,
+                                                      vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -282,6 +285,14 @@ def branch_decode(pool: KVPool, batch: Batch, Hq: int, q, k_new, v_new, tree_bit
     _check(lib().padoc_branch_decode(pool.handle, C.byref(batch.c), Hq, _ptr(q), _ptr(k_new), _ptr(v_new),
                                      _ptr(tree_bits), _ptr(o), _ptr(lse), float(scale), _ptr(ws), int(ws_bytes),
                                      _stream(stream)))
+
+
+def branch_decode_noalloc(pool: KVPool, batch: Batch, Hq: int, q, k_new, v_new, tree_bits, o, lse,
+                          scale: float = 0.0, stream=None):
+    """padoc_branch_decode with the workspace taken from the library's fixed
+    device array (no device allocation; for callers that may not allocate)."""
+    _check(lib().padoc_branch_decode_noalloc(pool.handle, C.byref(batch.c), Hq, _ptr(q), _ptr(k_new), _ptr(v_new),
+                                             _ptr(tree_bits), _ptr(o), _ptr(lse), float(scale), _stream(stream)))
 
 
 class DecodePlan:
