@@ -32,9 +32,21 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "branch-decode attn tokens/s & % HBM roofline; tree-varlen fwd TFLOP/s & % peak"
-WORKLOAD = ("serving-scale: branch decode over 512 pages (prefix U[4000,6144], 8-60 branches/page, "
-            "own suffix U[0,1024], 1 query/branch) + tree-varlen forward over 8 x 16384 packed tokens; "
-            "bf16, Hq=16, Hkv=8, d=128")
+WORKLOADS = {
+    "serving": "serving-scale: branch decode over 512 pages (prefix U[4000,6144], 8-60 branches/page, own suffix "
+               "U[0,1024], 1 query/branch)",
+    "branch": "branch decode over 16 pages (prefix 4809, 8-40 branches/page, own suffix U[0,512], 1 query/branch)",
+    "verify": "speculative verify over 64 pages (prefix 4809, 8-40 branches/page, own suffix U[0,512], draft tree "
+              "of up to 16 nodes per branch)",
+}
+
+
+def workload_name(kind: str, fwd_seqs: int) -> str:
+    return (WORKLOADS[kind] + f" + tree-varlen forward over {fwd_seqs} x 16384 packed tokens; bf16, Hq=16, "
+            "Hkv=8, d=128")
+
+
+WORKLOAD = workload_name("serving", 8)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -223,6 +235,9 @@ def main() -> int:
     ap.add_argument("--cpu-pages", type=int, default=32, help="decode pages in the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="serving", choices=sorted(WORKLOADS),
+                    help="serving (the default bench line); branch and verify are smaller cases for profiling")
+    ap.add_argument("--fwd-seqs", type=int, default=8, help="packed 16384-token sequences in the forward")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -234,7 +249,7 @@ def main() -> int:
 
     # the CPU baseline's process pool runs before any CUDA work (spawn)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "serving":
         cpu = cpu_oracle_baseline(args.seed, args.cpu_pages, 64)
 
     import torch
@@ -248,9 +263,9 @@ def main() -> int:
         build.build()
     seed = args.seed + 1000 * rank  # independent pages per rank
 
-    dw = wl.serving_decode(seed)
-    fw = wl.packed_sequences(seed)
-    dec = harness.Decode(dw, seed=seed, tree=False)
+    dw = {"serving": wl.serving_decode, "branch": wl.branch_decode, "verify": wl.spec_verify}[args.workload](seed)
+    fw = wl.packed_sequences(seed, n_seq=args.fwd_seqs)
+    dec = harness.Decode(dw, seed=seed, tree=args.workload == "verify")
     fwd = harness.Forward(fw, seed=seed)
     dec.plan()
     stream = torch.cuda.current_stream()
@@ -309,7 +324,7 @@ def main() -> int:
             d_q.copy_(h_q, non_blocking=True)
             d_k.copy_(h_k, non_blocking=True)
             d_v.copy_(h_v, non_blocking=True)
-            padoc.branch_decode(dec.pool, dec.batch, dw.Hq, d_q, d_k, d_v, None, dec.o, dec.lse, dec.ws,
+            padoc.branch_decode(dec.pool, dec.batch, dw.Hq, d_q, d_k, d_v, dec.tree_bits, dec.o, dec.lse, dec.ws,
                                 dec.ws_bytes)
             h_o.copy_(dec.o, non_blocking=True)
             h_l.copy_(dec.lse, non_blocking=True)
@@ -359,7 +374,7 @@ def main() -> int:
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "pages": len(dw.pages), "branches": dw.n_branches, "query_tokens": nq,
+        "config": {"workload": workload_name(args.workload, args.fwd_seqs), "pages": len(dw.pages), "branches": dw.n_branches, "query_tokens": nq,
                    "forward_tokens": fw.n_tokens,
                    "l2": "inputs larger than L2 (decode KV about 48 GB, forward Q/K/V 1.3 GB)",
                    "step": ("value and ms_per_step cover the decode step (prefix pass + own pass); the forward "

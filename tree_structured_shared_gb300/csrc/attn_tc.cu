@@ -55,7 +55,9 @@ constexpr int SM_K = SM_Q + 2 * kHalf;
 constexpr int SM_V = SM_K + kStages * 2 * kHalf;
 constexpr int SM_P = SM_V + kStages * 2 * kHalf;
 constexpr int SM_BAR = SM_P + 2 * 2 * kHalf;
-constexpr int SM_TOTAL = SM_BAR + 256;
+constexpr int SM_IDS = SM_BAR + 256;  // prefix pass: block ids of the unit's chunk
+constexpr int kMaxChunkBlocks = 384;
+constexpr int SM_TOTAL = SM_IDS + kMaxChunkBlocks * 4;
 constexpr int kSmemBytes = SM_TOTAL + 1024;
 
 // barrier slots
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && MODE == MODE_FWD) {
+    if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -264,22 +266,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                           w.tile_start);
         }
       } else {
-        // gather the page's query rows: row R = query (R / G), head g*G + R % G
-        const uint4* q4 = reinterpret_cast<const uint4*>(p.q);
-        for (int x = lane; x < kTileRows * 16; x += 32) {
-          const int r = x >> 4, c = x & 15;
-          uint4 val = make_uint4(0, 0, 0, 0);
-          if (r < w.rows) {
-            const int R = w.tile * kTileRows + r;
-            const int64_t qi = w.q_first + R / G;
-            const int head = w.g * G + R % G;
-            val = q4[(qi * p.Hq + head) * 16 + c];
-          }
-          *reinterpret_cast<uint4*>(smem + SM_Q + sw128_off(r, c)) = val;
+        // Query rows of the page, row R = (query R / G, head g*G + R % G): a
+        // 4-D box {d/2, G, 1, 128/G} of q viewed as [nq][Hkv][G][d] lands in
+        // exactly that row order.
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * kHalf);
+          for (int h = 0; h < 2; ++h)
+            tma_load_4d(sbase + SM_Q + h * kHalf, &tm_q, bar(B_Q_FULL), h * 64, 0, w.g,
+                        w.q_first + w.tile * (kTileRows / G));
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_Q_FULL));
+        // block ids of the whole chunk, read once per unit
+        {
+          int32_t* ids = reinterpret_cast<int32_t*>(smem + SM_IDS);
+          const int n_ids = (w.k_end - w.k_begin + 15) >> 4;
+          const int32_t* row = p.table + static_cast<int64_t>(w.seq) * p.max_bps + (w.k_begin >> 4);
+          for (int i = lane; i < n_ids; i += 32) ids[i] = row[i];
+          __syncwarp();
+        }
       }
       TileIter t;
       bool failed = false;
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
           int32_t blk = 0;
-          if (lane < nblk) blk = p.table[static_cast<int64_t>(w.seq) * p.max_bps + (t.ks >> 4) + lane];
+          if (lane < nblk) blk = reinterpret_cast<const int32_t*>(smem + SM_IDS)[((t.ks - w.k_begin) >> 4) + lane];
           if (lane == 0) mbar_arrive_expect_tx(bar(B_K_FULL + st), nblk * 2 * 2048);
           __syncwarp();
           if (lane < nblk) {
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
           int32_t blk = 0;
-          if (lane < nblk) blk = p.table[static_cast<int64_t>(w.seq) * p.max_bps + (t.ks >> 4) + lane];
+          if (lane < nblk) blk = reinterpret_cast<const int32_t*>(smem + SM_IDS)[((t.ks - w.k_begin) >> 4) + lane];
           if (lane == 0) mbar_arrive_expect_tx(bar(B_V_FULL + st), nblk * 2 * 2048);
           __syncwarp();
           if (lane < nblk) {
@@ -459,9 +462,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= vis) s[c] = -INFINITY;
         }
-        float tmax = s[0];
+        float tmax;
+        {
+          float m8[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) tmax = fmaxf(tmax, s[c]);
+          for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+          for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+          tmax = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        }
         const float mt = tmax * p.sl2;
         const bool grow = mt > m_run + kRescaleThreshold;
         const float alpha = grow ? fast_exp2(m_run - mt) : 1.f;  // 0 while m_run is -inf
@@ -470,13 +479,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mt;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float lsum = 0.f;
+        {
+          float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          s[c] = fast_exp2(fmaf(s[c], p.sl2, -m_use));
-          lsum += s[c];
+          for (int c = 0; c < 128; ++c) {
+            s[c] = fast_exp2(fmaf(s[c], p.sl2, -m_use));
+            l8[c & 7] += s[c];
+          }
+          l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         }
-        l_run += lsum;
         // Every P V product completes one O_DONE phase; wait for each one in
         // order (a parity wait is only sound one phase behind).  Once P V of
         // tile j-1 is done, O is stable and both P buffers are free.
@@ -562,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int make_map(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
              const cuuint64_t* strides, const cuuint32_t* box, std::string* err) {
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -630,11 +641,17 @@ int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   if (a.n_items == 0) return PADOC_OK;
   EncodeTiledFn enc = get_encode_fn(err);
   if (!enc) return PADOC_ERR_CUDA;
-  CUtensorMap mk, mv;
+  CUtensorMap mq, mk, mv;
+  // q viewed as [nq][Hkv][G][d]; box {64, G, 1, 128/G}
+  const cuuint64_t dq[4] = {128, static_cast<cuuint64_t>(a.group), static_cast<cuuint64_t>(a.Hkv),
+                            static_cast<cuuint64_t>(a.nq)};
+  const cuuint64_t sq[3] = {256, static_cast<cuuint64_t>(a.group) * 256, static_cast<cuuint64_t>(a.Hq) * 256};
+  const cuuint32_t bq[4] = {64, static_cast<cuuint32_t>(a.group), 1, static_cast<cuuint32_t>(kTileRows / a.group)};
   const cuuint64_t dk[2] = {128, static_cast<cuuint64_t>(a.num_blocks) * a.Hkv * 16};
   const cuuint64_t sk[1] = {256};
   const cuuint32_t bk[2] = {64, 16};
-  int rc = make_map(enc, &mk, a.k_pool, 2, dk, sk, bk, err);
+  int rc = make_map(enc, &mq, a.q, 4, dq, sq, bq, err);
+  if (!rc) rc = make_map(enc, &mk, a.k_pool, 2, dk, sk, bk, err);
   if (!rc) rc = make_map(enc, &mv, a.v_pool, 2, dk, sk, bk, err);
   if (rc) return rc;
   Params p{};
@@ -652,7 +669,7 @@ int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
-  return launch<MODE_PREFIX>(mk, mk, mv, p, s, err);
+  return launch<MODE_PREFIX>(mq, mk, mv, p, s, err);
 }
 
 int read_and_clear_tc_error(cudaStream_t s, unsigned* word) {
