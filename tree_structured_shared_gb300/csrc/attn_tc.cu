@@ -17,18 +17,20 @@
 //                branches (HPD-Parsing: forked branches share the prefix KV
 //                with zero copy).  Writes normalised partial O and LSE.
 //
-// Roles (192 threads):
+// Roles (224 threads):
 //   warps 0-3  softmax: thread r owns TMEM lane r = query row r.  Reads S from
-//              TMEM, masks, keeps the running max / sum, writes P (bf16) to
-//              shared memory, rescales O in TMEM when the max grows by more
-//              than 2^8, and runs the epilogue.
-//   warp 4     producer: TMA loads of Q (or a gather for decode rows), K, V.
+//              TMEM, masks, keeps the running max / sum, writes P (bf16 pairs)
+//              back over the S tile in TMEM, rescales O in TMEM when the max
+//              grows by more than 2^8, and runs the epilogue.
+//   warp 4     producer of Q and K tiles (TMA); decode: also stages the
+//              chunk's block ids in shared memory.
+//   warp 6     producer of V tiles (TMA), so K never waits behind V.
 //   warp 5     MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
-//              tile, O += P V into a TMEM accumulator.
+//              tile, O += P V (P read from TMEM) into a TMEM accumulator.
 //
 // TMEM: columns [0,128) and [128,256) hold S, [256,384) hold O (f32).
 // Shared memory (1024-byte aligned, 128-byte swizzle, two 64-column halves):
-//   Q 32 KB | K 2 x 32 KB | V 2 x 32 KB | P 2 x 32 KB | barriers.
+//   Q 32 KB | K 3 x 32 KB | V 3 x 32 KB | barriers | block ids.
 // Every wait is bounded; a unit that times out raises the CTA abort flag, the
 // device error word, and all roles leave their loops.
 #include <cuda_bf16.h>
@@ -47,14 +49,15 @@ using namespace ptx;
 
 enum { MODE_FWD = 0, MODE_PREFIX = 1 };
 
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kKStages = 3;  // K tiles in flight: S of tile j+1 needs K early
+constexpr int kVStages = 3;  // V tiles are consumed one softmax later
+constexpr int kThreads = 224;
 constexpr int kHalf = 16384;  // bytes of one 64-column half of a 128-row tile
 constexpr int SM_Q = 0;
 constexpr int SM_K = SM_Q + 2 * kHalf;
-constexpr int SM_V = SM_K + kStages * 2 * kHalf;
-constexpr int SM_P = SM_V + kStages * 2 * kHalf;
-constexpr int SM_BAR = SM_P + 2 * 2 * kHalf;
+constexpr int SM_V = SM_K + kKStages * 2 * kHalf;
+constexpr int SM_P = SM_V + kVStages * 2 * kHalf;
+constexpr int SM_BAR = SM_P;  // P lives in tensor memory, over the S tile it came from
 constexpr int SM_IDS = SM_BAR + 256;  // prefix pass: block ids of the unit's chunk
 constexpr int kMaxChunkBlocks = 384;
 constexpr int SM_TOTAL = SM_IDS + kMaxChunkBlocks * 4;
@@ -64,17 +67,17 @@ constexpr int kSmemBytes = SM_TOTAL + 1024;
 enum {
   B_Q_FULL = 0,
   B_Q_EMPTY = 1,
-  B_K_FULL = 2,   // +stage
-  B_K_EMPTY = 4,  // +stage
-  B_V_FULL = 6,
-  B_V_EMPTY = 8,
-  B_S_FULL = 10,  // +buffer
-  B_S_FREE = 12,
-  B_P_FULL = 14,
-  B_SPARE = 16,  // two unused slots
-  B_O_DONE = 18,
-  B_O_FREE = 19,
-  N_BARS = 20
+  B_K_FULL = 2,   // +stage (3)
+  B_K_EMPTY = 5,  // +stage (3)
+  B_V_FULL = 8,   // +stage (3)
+  B_V_EMPTY = 11, // +stage (3)
+  B_S_FULL = 14,  // +buffer (2)
+  B_P_FULL = 16,
+  B_O_DONE = 17,
+  B_O_FREE = 18,
+  B_IDS_READY = 19,  // prefix pass: the chunk's block ids are staged
+  B_IDS_FREE = 20,   // prefix pass: the V producer is done with them
+  N_BARS = 21
 };
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t cnt = 1;
-      if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_FREE) cnt = 4;
+      if (i == B_P_FULL || i == B_O_FREE) cnt = 4;
       mbar_init(bar(i), cnt);
     }
     *abort = 0;
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (MODE == MODE_PREFIX) {
     // stale bytes in a partly filled K/V tile are masked, but must be finite
     uint4 z = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < (SM_P - SM_K) / 16; i += kThreads)
+    for (int i = threadIdx.x; i < (SM_BAR - SM_K) / 16; i += kThreads)
       reinterpret_cast<uint4*>(smem + SM_K)[i] = z;
     fence_proxy_async_smem();
   }
@@ -241,101 +244,88 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int G = p.group;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------------------------ producers
+    // warp 4: Q and K (and, for the prefix pass, the chunk's block ids);
+    // warp 6: V.  Separate warps keep K loads from queueing behind V waits.
+    const bool is_k = warp == 4;
+    const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+    const int stages = is_k ? kKStages : kVStages;
+    const int b_full = is_k ? B_K_FULL : B_V_FULL;
+    const int b_empty = is_k ? B_K_EMPTY : B_V_EMPTY;
+    const uint32_t sm_base = sbase + (is_k ? SM_K : SM_V);
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+      if (is_k) tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(tm);
     }
-    uint32_t kv_it = 0, item_it = 0;
-    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+    int32_t* ids = reinterpret_cast<int32_t*>(smem + SM_IDS);
+    uint32_t it = 0, item_it = 0;
+    bool failed = false;
+    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
       const Unit w = load_unit(p, u);
       if (count_tiles(p, w) == 0) continue;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (item_it & 1) ^ 1, abort))) {
-        if (lane == 0) raise_abort(abort, 0x1);
-        break;
-      }
-      if (MODE == MODE_FWD) {
+      if (is_k) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (item_it & 1) ^ 1, abort))) { failed = true; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * kHalf);
-          const int tt = p.plan.tile_tokens;
-          for (int hh = 0; hh < G; ++hh)
+          if (MODE == MODE_FWD) {
+            const int tt = p.plan.tile_tokens;
+            for (int hh = 0; hh < G; ++hh)
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d(sbase + SM_Q + h * kHalf + hh * tt * 128, &tm_q, bar(B_Q_FULL), h * 64, w.g * G + hh,
+                            w.tile_start);
+          } else {
+            // Query rows of the page, row R = (query R / G, head g*G + R % G):
+            // a 4-D box {d/2, G, 1, 128/G} of q viewed as [nq][Hkv][G][d]
+            // lands in exactly that row order.
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(sbase + SM_Q + h * kHalf + hh * tt * 128, &tm_q, bar(B_Q_FULL), h * 64, w.g * G + hh,
-                          w.tile_start);
+              tma_load_4d(sbase + SM_Q + h * kHalf, &tm_q, bar(B_Q_FULL), h * 64, 0, w.g,
+                          w.q_first + w.tile * (kTileRows / G));
+          }
         }
-      } else {
-        // Query rows of the page, row R = (query R / G, head g*G + R % G): a
-        // 4-D box {d/2, G, 1, 128/G} of q viewed as [nq][Hkv][G][d] lands in
-        // exactly that row order.
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * kHalf);
-          for (int h = 0; h < 2; ++h)
-            tma_load_4d(sbase + SM_Q + h * kHalf, &tm_q, bar(B_Q_FULL), h * 64, 0, w.g,
-                        w.q_first + w.tile * (kTileRows / G));
-        }
-        // block ids of the whole chunk, read once per unit
-        {
-          int32_t* ids = reinterpret_cast<int32_t*>(smem + SM_IDS);
+        if (MODE == MODE_PREFIX) {
+          // block ids of the whole chunk, read once per unit and shared with warp 6
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_IDS_FREE), (item_it & 1) ^ 1, abort))) { failed = true; break; }
           const int n_ids = (w.k_end - w.k_begin + 15) >> 4;
           const int32_t* row = p.table + static_cast<int64_t>(w.seq) * p.max_bps + (w.k_begin >> 4);
           for (int i = lane; i < n_ids; i += 32) ids[i] = row[i];
           __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_IDS_READY));
         }
+      } else if (MODE == MODE_PREFIX) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_IDS_READY), item_it & 1, abort))) { failed = true; break; }
       }
       TileIter t;
-      bool failed = false;
-      for (bool ok = tiles_begin(p, w, t); ok; ok = tiles_next(p, w, t), ++kv_it) {
-        const int st = kv_it % kStages;
-        const uint32_t ph = ((kv_it / kStages) & 1) ^ 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_K_EMPTY + st), ph, abort))) { failed = true; break; }
+      for (bool ok = tiles_begin(p, w, t); ok; ok = tiles_next(p, w, t), ++it) {
+        const int st = it % stages;
+        const uint32_t ph = ((it / stages) & 1) ^ 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(b_empty + st), ph, abort))) { failed = true; break; }
+        const uint32_t dst = sm_base + st * 2 * kHalf;
         if (MODE == MODE_FWD) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(bar(B_K_FULL + st), 2 * kHalf);
-            for (int h = 0; h < 2; ++h)
-              tma_load_3d(sbase + SM_K + st * 2 * kHalf + h * kHalf, &tm_k, bar(B_K_FULL + st), h * 64, w.g, t.ks);
+            mbar_arrive_expect_tx(bar(b_full + st), 2 * kHalf);
+            for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kHalf, tm, bar(b_full + st), h * 64, w.g, t.ks);
           }
         } else {
           const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
           int32_t blk = 0;
-          if (lane < nblk) blk = reinterpret_cast<const int32_t*>(smem + SM_IDS)[((t.ks - w.k_begin) >> 4) + lane];
-          if (lane == 0) mbar_arrive_expect_tx(bar(B_K_FULL + st), nblk * 2 * 2048);
+          if (lane < nblk) blk = ids[((t.ks - w.k_begin) >> 4) + lane];
+          if (lane == 0) mbar_arrive_expect_tx(bar(b_full + st), nblk * 2 * 2048);
           __syncwarp();
           if (lane < nblk) {
             const int32_t row = (blk * p.Hkv + w.g) * 16;
-            for (int h = 0; h < 2; ++h)
-              tma_load_2d(sbase + SM_K + st * 2 * kHalf + h * kHalf + lane * 2048, &tm_k, bar(B_K_FULL + st),
-                          h * 64, row);
-          }
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_V_EMPTY + st), ph, abort))) { failed = true; break; }
-        if (MODE == MODE_FWD) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(bar(B_V_FULL + st), 2 * kHalf);
-            for (int h = 0; h < 2; ++h)
-              tma_load_3d(sbase + SM_V + st * 2 * kHalf + h * kHalf, &tm_v, bar(B_V_FULL + st), h * 64, w.g, t.ks);
-          }
-        } else {
-          const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
-          int32_t blk = 0;
-          if (lane < nblk) blk = reinterpret_cast<const int32_t*>(smem + SM_IDS)[((t.ks - w.k_begin) >> 4) + lane];
-          if (lane == 0) mbar_arrive_expect_tx(bar(B_V_FULL + st), nblk * 2 * 2048);
-          __syncwarp();
-          if (lane < nblk) {
-            const int32_t row = (blk * p.Hkv + w.g) * 16;
-            for (int h = 0; h < 2; ++h)
-              tma_load_2d(sbase + SM_V + st * 2 * kHalf + h * kHalf + lane * 2048, &tm_v, bar(B_V_FULL + st),
-                          h * 64, row);
+            for (int h = 0; h < 2; ++h) tma_load_2d(dst + h * kHalf + lane * 2048, tm, bar(b_full + st), h * 64, row);
           }
         }
       }
-      if (failed) {
-        if (lane == 0) raise_abort(abort, 0x2);
-        break;
+      if (failed) break;
+      if (!is_k && MODE == MODE_PREFIX) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_IDS_FREE));
       }
       ++item_it;
     }
+    if (failed && lane == 0) raise_abort(abort, is_k ? 0x1 : 0x2);
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -345,10 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t k_it = 0, v_it = 0, s_it = 0, p_it = 0, item_it = 0;
       bool failed = false;
       auto issue_s = [&]() -> bool {
-        const int st = k_it % kStages;
+        const int st = k_it % kKStages;
         const int sb = s_it & 1;
-        if (!mbar_wait(bar(B_K_FULL + st), (k_it / kStages) & 1, abort)) return false;
-        if (!mbar_wait(bar(B_S_FREE + sb), ((s_it >> 1) & 1) ^ 1, abort)) return false;
+        // S buffer sb last held P of tile s_it - 2, read by a P V issued
+        // before this MMA by this thread (tcgen05.mma runs in issue order)
+        if (!mbar_wait(bar(B_K_FULL + st), (k_it / kKStages) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t qa = sbase + SM_Q;
         const uint32_t ka = sbase + SM_K + st * 2 * kHalf;
@@ -376,20 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mma_commit(bar(B_Q_EMPTY));
           }
-          const int st = v_it % kStages;
-          const int pb = p_it & 1;
+          const int st = v_it % kVStages;
           if (j == 0 && !mbar_wait(bar(B_O_FREE), (item_it & 1) ^ 1, abort)) { failed = true; break; }
-          if (!mbar_wait(bar(B_P_FULL + pb), (p_it >> 1) & 1, abort)) { failed = true; break; }
-          if (!mbar_wait(bar(B_V_FULL + st), (v_it / kStages) & 1, abort)) { failed = true; break; }
+          if (!mbar_wait(bar(B_P_FULL), p_it & 1, abort)) { failed = true; break; }
+          if (!mbar_wait(bar(B_V_FULL + st), (v_it / kVStages) & 1, abort)) { failed = true; break; }
           tc_fence_after();
-          const uint32_t pa = sbase + SM_P + pb * 2 * kHalf;
+          const uint32_t pt = tmem + (p_it & 1) * 128;  // P (bf16 pairs) over S of this tile
           const uint32_t va = sbase + SM_V + st * 2 * kHalf;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-            mma_bf16_ss(t_o, sdesc_sw128(pa + aoff, 16, 1024), sdesc_sw128(va + kk * 2048, kHalf, 1024), id_pv,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(t_o, pt + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(B_V_EMPTY + st));
           mma_commit(bar(B_O_DONE));
           ++v_it;
@@ -445,9 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_S_FREE + sb));
         ++s_it;
         // mask keys this row may not see
         const int32_t klen = min(kTileKeys, t.end - t.ks);
@@ -508,17 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
         }
-        const int pb = p_it & 1;
-        const uint32_t pa = sbase + SM_P + pb * 2 * kHalf;
+        {
+          // P as bf16 pairs into the first 64 columns of this tile's S buffer
+          uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_shared_v4(pa + sw128_off(r, c), pack_bf16x2(s[8 * c + 0], s[8 * c + 1]),
-                       pack_bf16x2(s[8 * c + 2], s[8 * c + 3]), pack_bf16x2(s[8 * c + 4], s[8 * c + 5]),
-                       pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
-        fence_proxy_async_smem();
+          for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+          tmem_st64(tmem + lane_base + sb * 128, pk);
+          tmem_wait_st();
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_P_FULL + pb));
+        if (lane == 0) mbar_arrive(bar(B_P_FULL));
         ++p_it;
       }
       if (failed) break;
