@@ -385,7 +385,8 @@ def main() -> int:
                      "traffic": traffic_for("own_pass", own_units), "algorithmic_bytes": own_b, "ms": t_own},
         "kernels": {
             "prefix_pass": {"ms": t_pre, "achieved_gbs": pre_gbs, "frac_hbm": pre_gbs / hbm,
-                            "algorithmic_bytes": pre_b},
+                            "algorithmic_bytes": pre_b,
+                            "traffic": traffic_for("prefix_pass", sum(max(p.branch_prefix_len or [0]) for p in dw.pages))},
             "own_pass": {"ms": t_own, "achieved_gbs": own_gbs, "frac_hbm": own_gbs / hbm,
                          "algorithmic_bytes": own_b},
             "decode_step": {"ms": t_dec, "achieved_gbs": dec_gbs, "frac_hbm": dec_gbs / hbm,
