@@ -18,7 +18,8 @@
 //                with zero copy).  Writes normalised partial O and LSE.
 //
 // Roles (224 threads):
-//   warps 0-3  softmax: thread r owns TMEM lane r = query row r.  Reads S from
+//   warps 0-3  softmax: thread r owns TMEM lane r = query row r.  Copies its
+//              Q row into TMEM at the start of a unit.  Reads S from
 //              TMEM, masks, keeps the running max / sum, writes P (bf16 pairs)
 //              back over the S tile in TMEM, rescales O in TMEM when the max
 //              grows by more than 2^8, and runs the epilogue.
@@ -28,7 +29,9 @@
 //   warp 5     MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
 //              tile, O += P V (P read from TMEM) into a TMEM accumulator.
 //
-// TMEM: columns [0,128) and [128,256) hold S, [256,384) hold O (f32).
+// TMEM: columns [0,128) and [128,256) hold S (then P), [256,384) hold O
+// (f32), [384,448) hold Q as bf16 pairs, so both MMAs read A from TMEM and
+// only K and V come from shared memory.
 // Shared memory (1024-byte aligned, 128-byte swizzle, two 64-column halves):
 //   Q 32 KB | K 3 x 32 KB | V 3 x 32 KB | barriers | block ids.
 // Every wait is bounded; a unit that times out raises the CTA abort flag, the
@@ -77,10 +80,12 @@ enum {
   B_O_FREE = 18,
   B_IDS_READY = 19,  // prefix pass: the chunk's block ids are staged
   B_IDS_FREE = 20,   // prefix pass: the V producer is done with them
-  N_BARS = 21
+  B_QT_FULL = 21,    // softmax warps copied Q into tensor memory
+  N_BARS = 22
 };
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kTmemQ = 384;           // TMEM columns [384, 448): Q as bf16 pairs
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t cnt = 1;
-      if (i == B_P_FULL || i == B_O_FREE) cnt = 4;
+      if (i == B_P_FULL || i == B_O_FREE || i == B_Q_EMPTY || i == B_QT_FULL) cnt = 4;
       mbar_init(bar(i), cnt);
     }
     *abort = 0;
@@ -341,13 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // before this MMA by this thread (tcgen05.mma runs in issue order)
         if (!mbar_wait(bar(B_K_FULL + st), (k_it / kKStages) & 1, abort)) return false;
         tc_fence_after();
-        const uint32_t qa = sbase + SM_Q;
         const uint32_t ka = sbase + SM_K + st * 2 * kHalf;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          mma_bf16_ss(tmem + sb * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), id_qk,
-                      kk > 0);
+          mma_bf16_ts(tmem + sb * 128, tmem + kTmemQ + kk * 8, sdesc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
         }
         mma_commit(bar(B_S_FULL + sb));
         mma_commit(bar(B_K_EMPTY + st));
@@ -359,13 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit w = load_unit(p, u);
         const int n = count_tiles(p, w);
         if (n == 0) continue;
-        if (!mbar_wait(bar(B_Q_FULL), item_it & 1, abort)) { failed = true; break; }
+        if (!mbar_wait(bar(B_QT_FULL), item_it & 1, abort)) { failed = true; break; }
         if (!issue_s()) { failed = true; break; }
         for (int j = 0; j < n; ++j) {
           if (j + 1 < n) {
             if (!issue_s()) { failed = true; break; }
-          } else {
-            mma_commit(bar(B_Q_EMPTY));
           }
           const int st = v_it % kVStages;
           if (j == 0 && !mbar_wait(bar(B_O_FREE), (item_it & 1) ^ 1, abort)) { failed = true; break; }
@@ -390,12 +391,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax (warps 0-3)
     const int r = threadIdx.x;  // query row == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t s_it = 0, p_it = 0, pv_base = 0;
+    uint32_t s_it = 0, p_it = 0, pv_base = 0, unit_it = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
       const Unit w = load_unit(p, u);
       const int n = count_tiles(p, w);
       if (n == 0) continue;
+      // Q row r into tensor memory as bf16 pairs (the A operand of S = Q K^T).
+      // Every S MMA of the previous unit has completed: this warp consumed
+      // all of their S tiles.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL), unit_it & 1, abort))) { failed = true; break; }
+      {
+        uint32_t qk[64];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(smem + SM_Q + sw128_off(r, c));
+          qk[4 * c + 0] = v4.x;
+          qk[4 * c + 1] = v4.y;
+          qk[4 * c + 2] = v4.z;
+          qk[4 * c + 3] = v4.w;
+        }
+        tmem_st64(tmem + lane_base + kTmemQ, qk);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_QT_FULL));
+        mbar_arrive(bar(B_Q_EMPTY));
+      }
+      ++unit_it;
       // this thread's row
       bool valid;
       int32_t head, limit;  // limit: keys at positions >= limit are hidden (prefix) / causal bound (fwd)
