@@ -146,3 +146,17 @@ def test_repeat_decode_bit_identical(harness):
         torch.cuda.synchronize()
         assert torch.equal(d.o, o0) and torch.equal(d.lse, l0)
     padoc.device_status()
+
+
+def test_cuda_core_own_pass_short_blocks(harness):
+    """G = 1 with 1-3 query tokens per branch stays on the CUDA-core own pass
+    (fewer than 4 rows per branch and kv head on average)."""
+    rng = np.random.default_rng(12)
+    pages = []
+    for _ in range(3):
+        N = int(rng.integers(2, 6))
+        par = [[-1] + list(range(int(rng.integers(0, 2)))) for _ in range(N)]
+        pages.append(wl.DecodePage(300, [300] * N, rng.integers(0, 90, N).tolist(), [len(t) for t in par], par))
+    w = wl.DecodeWorkload("short", pages, 2, 2, 128, 1.0)
+    og, lg, O, L = _decode(harness, w, 12)
+    check(og, lg, O, L, "bf16", "short blocks")

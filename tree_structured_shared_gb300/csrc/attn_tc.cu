@@ -50,7 +50,7 @@ namespace {
 
 using namespace ptx;
 
-enum { MODE_FWD = 0, MODE_PREFIX = 1 };
+enum { MODE_FWD = 0, MODE_PREFIX = 1, MODE_OWN = 2 };
 
 constexpr int kKStages = 3;  // K tiles in flight: S of tile j+1 needs K early
 constexpr int kVStages = 3;  // V tiles are consumed one softmax later
@@ -108,6 +108,9 @@ struct Params {
   const __nv_bfloat16* q;
   float* part_o;
   float* part_lse;
+  // own pass
+  const DecBranch* branches;
+  const uint16_t* tree_bits;
 };
 
 // The work unit as seen by every role (computed identically by each).
@@ -115,8 +118,10 @@ struct Unit {
   int32_t g;         // kv head
   // forward
   int32_t tile_start, q_end, kv_first, kv_count, tile_last;
-  // prefix
+  // prefix / own
   int32_t page, tile, rows, row_base, k_begin, k_end, seq, q_first;
+  // own
+  int32_t own_len, n_shared, q_len, q_in_page;
 };
 
 __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
@@ -131,6 +136,16 @@ __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
     w.kv_first = qs.kv_first;
     w.kv_count = qs.kv_count;
     w.tile_last = min(it.tile_start + p.plan.tile_tokens, w.q_end) - 1;
+  } else if (p.mode == MODE_OWN) {
+    const DecBranch br = p.branches[item];
+    w.page = br.page;
+    w.seq = br.seq;
+    w.q_first = br.q_first;
+    w.own_len = br.own_len;
+    w.n_shared = br.n_shared;
+    w.q_len = br.q_len;
+    w.q_in_page = br.q_in_page;
+    w.rows = br.q_len * p.group;
   } else {
     const DecItem it = p.items[item];
     const DecPage pg = p.pages[it.page];
@@ -173,6 +188,16 @@ __device__ __forceinline__ bool tiles_begin(const Params& p, const Unit& w, Tile
     t.s_end = w.kv_first + w.kv_count;
     return seg_setup(p, w, t);
   }
+  if (p.mode == MODE_OWN) {
+    // the branch's own cached tokens (t.s == 0), then one tile of the query
+    // block's own keys (t.s == 1)
+    t.s = w.own_len > 0 ? 0 : 1;
+    t.s_end = 2;
+    t.ks = 0;
+    t.end = w.own_len > 0 ? w.own_len : w.q_len;
+    t.causal = 0;
+    return true;
+  }
   t.s = 0;
   t.s_end = 1;
   t.ks = w.k_begin;
@@ -187,6 +212,12 @@ __device__ __forceinline__ bool tiles_next(const Params& p, const Unit& w, TileI
   if (p.mode == MODE_FWD) {
     ++t.s;
     return seg_setup(p, w, t);
+  }
+  if (p.mode == MODE_OWN && t.s == 0) {
+    t.s = 1;
+    t.ks = 0;
+    t.end = w.q_len;
+    return true;
   }
   return false;
 }
@@ -212,7 +243,8 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kn,
+                   const __grid_constant__ CUtensorMap tm_vn, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -232,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort = 0;
     fence_mbar_init();
   }
-  if (MODE == MODE_PREFIX) {
+  if (MODE != MODE_FWD) {
     // stale bytes in a partly filled K/V tile are masked, but must be finite
     uint4 z = make_uint4(0, 0, 0, 0);
     for (int i = threadIdx.x; i < (SM_BAR - SM_K) / 16; i += kThreads)
@@ -283,9 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Query rows of the page, row R = (query R / G, head g*G + R % G):
             // a 4-D box {d/2, G, 1, 128/G} of q viewed as [nq][Hkv][G][d]
             // lands in exactly that row order.
-            for (int h = 0; h < 2; ++h)
-              tma_load_4d(sbase + SM_Q + h * kHalf, &tm_q, bar(B_Q_FULL), h * 64, 0, w.g,
-                          w.q_first + w.tile * (kTileRows / G));
+            const int q0 = MODE == MODE_OWN ? w.q_first : w.q_first + w.tile * (kTileRows / G);
+            for (int h = 0; h < 2; ++h) tma_load_4d(sbase + SM_Q + h * kHalf, &tm_q, bar(B_Q_FULL), h * 64, 0, w.g, q0);
           }
         }
         if (MODE == MODE_PREFIX) {
@@ -311,10 +342,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar(b_full + st), 2 * kHalf);
             for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kHalf, tm, bar(b_full + st), h * 64, w.g, t.ks);
           }
+        } else if (MODE == MODE_OWN && t.s == 1) {
+          // the query block's own keys: 16 rows of k_new / v_new for kv head g
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(b_full + st), 2 * 2048);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(dst + h * kHalf, is_k ? &tm_kn : &tm_vn, bar(b_full + st), h * 64, w.g, w.q_first);
+          }
         } else {
           const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
           int32_t blk = 0;
-          if (lane < nblk) blk = ids[((t.ks - w.k_begin) >> 4) + lane];
+          if (MODE == MODE_OWN) {
+            if (lane < nblk)
+              blk = p.table[static_cast<int64_t>(w.seq) * p.max_bps + w.n_shared + (t.ks >> 4) + lane];
+          } else if (lane < nblk) {
+            blk = ids[((t.ks - w.k_begin) >> 4) + lane];
+          }
           if (lane == 0) mbar_arrive_expect_tx(bar(b_full + st), nblk * 2 * 2048);
           __syncwarp();
           if (lane < nblk) {
@@ -432,6 +475,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         valid = qpos < w.q_end;
         head = w.g * G + hh;
         limit = static_cast<int32_t>(qpos) + 1;
+      } else if (MODE == MODE_OWN) {
+        valid = r < w.rows;
+        head = w.g * G + r % G;
+        qpos = w.q_first + r / G;
+        limit = w.own_len;
       } else {
         valid = r < w.rows;
         const int R = w.tile * kTileRows + r;
@@ -463,10 +511,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t vis = klen;  // keys [0, vis) of the tile are visible
         if (MODE == MODE_FWD) {
           if (t.causal) vis = min(vis, limit - t.ks);
-        } else {
+        } else if (MODE == MODE_PREFIX) {
           vis = min(vis, limit - t.ks);
         }
-        if (vis < kTileKeys) {
+        if (MODE == MODE_OWN && t.s == 1) {
+          // query block: key c is query token c of this branch, visible iff it
+          // is this token's draft-tree ancestor or the token itself
+          const int qi = r / G;
+          uint32_t bits = 0;
+          if (valid) bits = p.tree_bits ? static_cast<uint32_t>(p.tree_bits[qpos]) : ((2u << qi) - 1u);
+          bits &= (1u << w.q_len) - 1u;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= 16 || !((bits >> c) & 1u)) s[c] = -INFINITY;
+        } else if (vis < kTileKeys) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c >= vis) s[c] = -INFINITY;
@@ -534,6 +592,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: O / l and LSE
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (pv_base + n - 1) & 1, abort))) { failed = true; break; }
       tc_fence_after();
+      if (MODE == MODE_OWN) {
+        // merge with the prefix pass's partial rows of this (query, head) by
+        // log-sum-exp, then write the final O and LSE
+        const DecPage pg = p.pages[w.page];
+        const int R = (w.q_in_page + r / G) * G + r % G;
+        const int ptile = R / kTileRows, prr = R % kTileRows;
+        float M = l_run > 0.f ? m_run : -INFINITY;
+        for (int c = 0; c < pg.n_chunks && valid; ++c) {
+          const DecItem it = p.items[pg.item_base + ptile * pg.n_chunks + c];
+          M = fmaxf(M, p.part_lse[static_cast<int64_t>(it.row_base) + static_cast<int64_t>(w.g) * it.rows + prr] * kLog2e);
+        }
+        const float Mu = M == -INFINITY ? 0.f : M;
+        const float w_own = l_run > 0.f ? fast_exp2(m_run - Mu) : 0.f;
+        float L = l_run * w_own;
+        for (int c = 0; c < pg.n_chunks && valid; ++c) {
+          const DecItem it = p.items[pg.item_base + ptile * pg.n_chunks + c];
+          L += fast_exp2(p.part_lse[static_cast<int64_t>(it.row_base) + static_cast<int64_t>(w.g) * it.rows + prr] *
+                             kLog2e - Mu);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tmem + 256 + lane_base + cc * 32, v);
+          tmem_wait_ld();
+          if (valid) {
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]) * w_own;
+            for (int c = 0; c < pg.n_chunks; ++c) {
+              const DecItem it = p.items[pg.item_base + ptile * pg.n_chunks + c];
+              const int64_t prow = static_cast<int64_t>(it.row_base) + static_cast<int64_t>(w.g) * it.rows + prr;
+              const float wc = fast_exp2(p.part_lse[prow] * kLog2e - Mu);
+              const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * kHeadDim + cc * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 x = src[i];
+                acc[4 * i + 0] = fmaf(x.x, wc, acc[4 * i + 0]);
+                acc[4 * i + 1] = fmaf(x.y, wc, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(x.z, wc, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(x.w, wc, acc[4 * i + 3]);
+              }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.o + (qpos * p.Hq + head) * kHeadDim + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(acc[8 * i + 0] * inv, acc[8 * i + 1] * inv),
+                                  pack_bf16x2(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
+                                  pack_bf16x2(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
+                                  pack_bf16x2(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_O_FREE));
+        if (valid) p.lse[qpos * p.Hq + head] = L > 0.f ? (Mu + __log2f(L)) * kLn2 : -INFINITY;
+        pv_base += n;
+        continue;
+      }
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
 #pragma unroll
@@ -594,9 +711,9 @@ int make_map(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, int rank, const
 }
 
 template <int MODE>
-int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm, cudaStream_t s,
-           std::string* err) {
-  static bool attr_set[2] = {false, false};
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mkn,
+           const CUtensorMap& mvn, const Params& prm, cudaStream_t s, std::string* err) {
+  static bool attr_set[3] = {false, false, false};
   if (!attr_set[MODE]) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) {
@@ -606,7 +723,7 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
     attr_set[MODE] = true;
   }
   const int grid = std::min(prm.n_units, num_sms());
-  attn_tc_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, prm);
+  attn_tc_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mkn, mvn, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *err = std::string("attention kernel launch: ") + cudaGetErrorString(e);
@@ -643,7 +760,7 @@ int launch_fwd_bf16(const FwdArgs& a, cudaStream_t s, std::string* err) {
   p.T = a.T;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
-  return launch<MODE_FWD>(mq, mk, mv, p, s, err);
+  return launch<MODE_FWD>(mq, mk, mv, mk, mv, p, s, err);
 }
 
 int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err) {
@@ -678,7 +795,50 @@ int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
-  return launch<MODE_PREFIX>(mq, mk, mv, p, s, err);
+  return launch<MODE_PREFIX>(mq, mk, mv, mk, mv, p, s, err);
+}
+
+int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err) {
+  if (a.n_branches == 0) return PADOC_OK;
+  EncodeTiledFn enc = get_encode_fn(err);
+  if (!enc) return PADOC_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mkn, mvn;
+  const cuuint64_t dq[4] = {128, static_cast<cuuint64_t>(a.group), static_cast<cuuint64_t>(a.Hkv),
+                            static_cast<cuuint64_t>(a.nq)};
+  const cuuint64_t sq[3] = {256, static_cast<cuuint64_t>(a.group) * 256, static_cast<cuuint64_t>(a.Hq) * 256};
+  const cuuint32_t bq[4] = {64, static_cast<cuuint32_t>(a.group), 1, static_cast<cuuint32_t>(kTileRows / a.group)};
+  const cuuint64_t dk[2] = {128, static_cast<cuuint64_t>(a.num_blocks) * a.Hkv * 16};
+  const cuuint64_t sk[1] = {256};
+  const cuuint32_t bk[2] = {64, 16};
+  // k_new / v_new viewed as [nq][Hkv][d]; box: 16 query tokens of one kv head
+  const cuuint64_t dn[3] = {128, static_cast<cuuint64_t>(a.Hkv), static_cast<cuuint64_t>(a.nq)};
+  const cuuint64_t sn[2] = {256, static_cast<cuuint64_t>(a.Hkv) * 256};
+  const cuuint32_t bn[3] = {64, 1, 16};
+  int rc = make_map(enc, &mq, a.q, 4, dq, sq, bq, err);
+  if (!rc) rc = make_map(enc, &mk, a.k_pool, 2, dk, sk, bk, err);
+  if (!rc) rc = make_map(enc, &mv, a.v_pool, 2, dk, sk, bk, err);
+  if (!rc) rc = make_map(enc, &mkn, a.k_new, 3, dn, sn, bn, err);
+  if (!rc) rc = make_map(enc, &mvn, a.v_new, 3, dn, sn, bn, err);
+  if (rc) return rc;
+  Params p{};
+  p.mode = MODE_OWN;
+  p.n_units = a.n_branches * a.Hkv;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.group = a.group;
+  p.sl2 = a.scale * kLog2e;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.pages = a.pages;
+  p.items = a.items;
+  p.table = a.table;
+  p.max_bps = a.max_bps;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.part_o = a.part_o;
+  p.part_lse = a.part_lse;
+  p.branches = a.branches;
+  p.tree_bits = a.tree_bits;
+  return launch<MODE_OWN>(mq, mk, mv, mkn, mvn, p, s, err);
 }
 
 int read_and_clear_tc_error(cudaStream_t s, unsigned* word) {

@@ -708,6 +708,7 @@ struct DecodePlan {
   std::vector<DecBranch> branches;
   std::vector<int32_t> q_plen;
   int64_t part_rows = 0;
+  bool tc_own = false;  // own pass on tensor cores (several query rows per branch and kv head)
   size_t off_pages = 0, off_items = 0, off_branches = 0, off_qplen = 0, off_part_o = 0, off_part_lse = 0,
          total = 0;
 };
@@ -808,6 +809,10 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
   }
   if (rows >= (int64_t(1) << 31)) return fail(PADOC_ERR_UNSUPPORTED, "branch_decode: batch too large");
   pl->part_rows = rows;
+  // One query token per branch gives G rows per (branch, kv head): the
+  // CUDA-core own pass streams that at HBM speed.  Draft-tree verify stacks
+  // up to 16 G rows, which needs the tensor-core own pass.
+  pl->tc_own = b->n_branches > 0 && static_cast<int64_t>(nq) * G >= 4 * static_cast<int64_t>(b->n_branches);
   size_t off = 0;
   pl->off_pages = off;
   off = align_up(off + pl->pages.size() * sizeof(DecPage), 256);
@@ -967,7 +972,8 @@ extern "C" int padoc_decode_own_pass(const padoc_decode_plan* plan, const void* 
   if (!plan->pool->d_table) return fail(PADOC_ERR_INVALID, "decode_own_pass: plan was not uploaded");
   const DecodeArgs a = decode_args(plan, q, k_new, v_new, tree_bits, o, lse, scale, ws);
   std::string err;
-  rc = launch_decode_own(a, reinterpret_cast<cudaStream_t>(stream), &err);
+  rc = plan->pl.tc_own ? launch_decode_own_tc(a, reinterpret_cast<cudaStream_t>(stream), &err)
+                       : launch_decode_own(a, reinterpret_cast<cudaStream_t>(stream), &err);
   if (rc) return fail(rc, "decode_own_pass: %s", err.c_str());
   return PADOC_OK;
 }

@@ -102,6 +102,7 @@ int launch_fwd_bf16(const FwdArgs& a, cudaStream_t s, std::string* err);
 int launch_fwd_f32(const FwdArgs& a, cudaStream_t s, std::string* err);
 int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err);
 int launch_decode_own(const DecodeArgs& a, cudaStream_t s, std::string* err);
+int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err);
 int launch_kv_append(void* k_pool, void* v_pool, const int32_t* table_row, int32_t first_own,
                      int32_t n, int32_t Hkv, int32_t d, const void* k, const void* v,
                      cudaStream_t s, std::string* err);
