@@ -25,7 +25,9 @@
 //              grows by more than 2^8, and runs the epilogue.
 //   warp 4     producer of Q and K tiles (TMA); decode: also stages the
 //              chunk's block ids in shared memory.
-//   warp 6     producer of V tiles (TMA), so K never waits behind V.
+//   warp 6     producer of V tiles (TMA).  K and V of a key tile share one
+//              ring stage and one full barrier, so the MMA thread waits once
+//              per tile for both.
 //   warp 5     MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
 //              tile, O += P V (P read from TMEM) into a TMEM accumulator.
 //
@@ -33,7 +35,7 @@
 // (f32), [384,448) hold Q as bf16 pairs, so both MMAs read A from TMEM and
 // only K and V come from shared memory.
 // Shared memory (1024-byte aligned, 128-byte swizzle, two 64-column halves):
-//   Q 32 KB | K 3 x 32 KB | V 3 x 32 KB | barriers | block ids.
+//   Q 32 KB | K 3 x 32 KB | V 3 x 32 KB (ring of 3 K/V stages) | barriers | block ids.
 // Every wait is bounded; a unit that times out raises the CTA abort flag, the
 // device error word, and all roles leave their loops.
 #include <cuda_bf16.h>
@@ -52,14 +54,13 @@ using namespace ptx;
 
 enum { MODE_FWD = 0, MODE_PREFIX = 1, MODE_OWN = 2 };
 
-constexpr int kKStages = 3;  // K tiles in flight: S of tile j+1 needs K early
-constexpr int kVStages = 3;  // V tiles are consumed one softmax later
+constexpr int kStages = 3;  // K/V tile ring; stage s holds K and V of the same key tile
 constexpr int kThreads = 224;
 constexpr int kHalf = 16384;  // bytes of one 64-column half of a 128-row tile
 constexpr int SM_Q = 0;
 constexpr int SM_K = SM_Q + 2 * kHalf;
-constexpr int SM_V = SM_K + kKStages * 2 * kHalf;
-constexpr int SM_P = SM_V + kVStages * 2 * kHalf;
+constexpr int SM_V = SM_K + kStages * 2 * kHalf;
+constexpr int SM_P = SM_V + kStages * 2 * kHalf;
 constexpr int SM_BAR = SM_P;  // P lives in tensor memory, over the S tile it came from
 constexpr int SM_IDS = SM_BAR + 256;  // prefix pass: block ids of the unit's chunk
 constexpr int kMaxChunkBlocks = 384;
@@ -70,10 +71,9 @@ constexpr int kSmemBytes = SM_TOTAL + 1024;
 enum {
   B_Q_FULL = 0,
   B_Q_EMPTY = 1,
-  B_K_FULL = 2,   // +stage (3)
-  B_K_EMPTY = 5,  // +stage (3)
-  B_V_FULL = 8,   // +stage (3)
-  B_V_EMPTY = 11, // +stage (3)
+  B_KV_FULL = 2,   // +stage (3): K and V of the stage landed (one arrival per producer)
+  B_KV_EMPTY = 5,  // +stage (3): P V of the stage's tile completed
+  B_SPARE = 8,     // six unused slots
   B_S_FULL = 14,  // +buffer (2)
   B_P_FULL = 16,
   B_O_DONE = 17,
@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t cnt = 1;
       if (i == B_P_FULL || i == B_O_FREE || i == B_Q_EMPTY || i == B_QT_FULL) cnt = 4;
+      if (i >= B_KV_FULL && i < B_KV_FULL + kStages) cnt = 2;
       mbar_init(bar(i), cnt);
     }
     *abort = 0;
@@ -287,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp 6: V.  Separate warps keep K loads from queueing behind V waits.
     const bool is_k = warp == 4;
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
-    const int stages = is_k ? kKStages : kVStages;
-    const int b_full = is_k ? B_K_FULL : B_V_FULL;
-    const int b_empty = is_k ? B_K_EMPTY : B_V_EMPTY;
+    const int stages = kStages;
+    const int b_full = B_KV_FULL;
+    const int b_empty = B_KV_EMPTY;
     const uint32_t sm_base = sbase + (is_k ? SM_K : SM_V);
     if (lane == 0) {
       if (is_k) tma_prefetch_desc(&tm_q);
@@ -383,11 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t k_it = 0, v_it = 0, s_it = 0, p_it = 0, item_it = 0;
       bool failed = false;
       auto issue_s = [&]() -> bool {
-        const int st = k_it % kKStages;
+        const int st = k_it % kStages;
         const int sb = s_it & 1;
         // S buffer sb last held P of tile s_it - 2, read by a P V issued
         // before this MMA by this thread (tcgen05.mma runs in issue order)
-        if (!mbar_wait(bar(B_K_FULL + st), (k_it / kKStages) & 1, abort)) return false;
+        // K and V of this tile (one wait for both; see mbar_try_wait_relaxed)
+        if (!mbar_wait_relaxed(bar(B_KV_FULL + st), (k_it / kStages) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t ka = sbase + SM_K + st * 2 * kHalf;
 #pragma unroll
@@ -396,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tmem + sb * 128, tmem + kTmemQ + kk * 8, sdesc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
         }
         mma_commit(bar(B_S_FULL + sb));
-        mma_commit(bar(B_K_EMPTY + st));
         ++k_it;
         ++s_it;
         return true;
@@ -405,23 +406,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit w = load_unit(p, u);
         const int n = count_tiles(p, w);
         if (n == 0) continue;
-        if (!mbar_wait(bar(B_QT_FULL), item_it & 1, abort)) { failed = true; break; }
+        if (!mbar_wait_relaxed(bar(B_QT_FULL), item_it & 1, abort)) { failed = true; break; }
         if (!issue_s()) { failed = true; break; }
         for (int j = 0; j < n; ++j) {
           if (j + 1 < n) {
             if (!issue_s()) { failed = true; break; }
           }
-          const int st = v_it % kVStages;
-          if (j == 0 && !mbar_wait(bar(B_O_FREE), (item_it & 1) ^ 1, abort)) { failed = true; break; }
-          if (!mbar_wait(bar(B_P_FULL), p_it & 1, abort)) { failed = true; break; }
-          if (!mbar_wait(bar(B_V_FULL + st), (v_it / kVStages) & 1, abort)) { failed = true; break; }
+          const int st = v_it % kStages;  // V landed with K, before S of this tile
+          if (j == 0 && !mbar_wait_relaxed(bar(B_O_FREE), (item_it & 1) ^ 1, abort)) { failed = true; break; }
+          if (!mbar_wait_relaxed(bar(B_P_FULL), p_it & 1, abort)) { failed = true; break; }
           tc_fence_after();
           const uint32_t pt = tmem + (p_it & 1) * 128;  // P (bf16 pairs) over S of this tile
           const uint32_t va = sbase + SM_V + st * 2 * kHalf;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(t_o, pt + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(B_V_EMPTY + st));
+          mma_commit(bar(B_KV_EMPTY + st));
           mma_commit(bar(B_O_DONE));
           ++v_it;
           ++p_it;
