@@ -257,6 +257,65 @@ PADOC_API int padoc_decode_plan_free(padoc_decode_plan* plan);
  * iff node j is node i or one of its ancestors.  Host arrays. */
 PADOC_API int padoc_tree_mask_build(const int32_t* parent, int32_t n, uint16_t* bits);
 
+/* ------------------------------------------------------------------------
+ * Accept step of speculative verify (HSD page, "greedy tree traversal";
+ * HPD-Parsing, inference workflow: accepted length n_acc of a drafted chain).
+ *
+ * The query rows [q_offsets[b], q_offsets[b+1]) of branch b are the nodes of
+ * its draft tree; node 0 is the anchor (the token fixed by the previous
+ * step) and row r of logits holds the model's next-token scores after node r.
+ * From the anchor the walk takes, among the current node's children, the one
+ * whose token scores highest (lowest node index on ties) and accepts it when
+ *     logit(child) - max(row) >= log(tau)            (float32 arithmetic)
+ * -- the log-probability difference of the HSD rule, whose softmax
+ * normaliser cancels -- and stops otherwise or at a leaf.  The free token is
+ * the argmax of the last accepted node's row (lowest token index on ties).
+ * tau = 1 is the greedy rule: a draft is kept while it is the argmax.
+ *
+ *   logits     device [nq, vocab] bf16, row-major, finite (NaN: unspecified)
+ *   tokens     device [nq] int32: token of each node (node 0's is not read)
+ *   parents    device [nq] int32: parent node index within the branch, -1
+ *              for node 0 and in [0, i) for node i >= 1
+ *   q_offsets  device [n_branches + 1] int32
+ *   max_nodes  host bound on nodes per branch, 1..16; each branch gets this
+ *              many argmax CTAs, so keep it tight (1 for plain decode)
+ *   tau        acceptance threshold, > 0 (0.75 in the HSD page)
+ *   n_acc      device [n_branches] int32 out: nodes accepted after the anchor
+ *   path       device [n_branches, 16] int32 out: accepted node indices in
+ *              order, -1 padded
+ *   free_token device [n_branches] int32 out
+ * A branch with no node or more than max_nodes nodes, rows outside [0, nq),
+ * a parent on node 0, a parent that is not an earlier node, or a token
+ * outside [0, vocab) gets n_acc = -1, free_token = -1 and a path of -1; the
+ * other branches are unaffected.  Host checks (null pointers, sizes, tau)
+ * return PADOC_ERR_INVALID before any launch.  Two launches on stream, no
+ * workspace: the row argmaxes are parked in path between them. */
+PADOC_API int padoc_verify_accept(const void* logits, int32_t nq, int32_t vocab, const int32_t* tokens,
+                                  const int32_t* parents, const int32_t* q_offsets, int32_t n_branches,
+                                  int32_t max_nodes, float tau, int32_t* n_acc, int32_t* path,
+                                  int32_t* free_token, padoc_stream_t stream);
+
+/* Commit of accepted draft tokens (HPD-Parsing, inference workflow: accepted
+ * tokens join the branch's own KV, rejected drafts never reach the cache).
+ * Appends to each listed sequence, in order, the rows of k_new / v_new that
+ * it names.  For a verified branch b the rows are usually its anchor
+ * q_offsets[b] followed by q_offsets[b] + path[b][0 .. n_acc[b]).
+ *   seqs        host [n_seqs]: distinct live sequences
+ *   row_offsets host [n_seqs + 1], row_offsets[0] = 0, non-decreasing:
+ *               sequence i takes rows[row_offsets[i] .. row_offsets[i+1])
+ *   rows        host: row indices into k_new / v_new, each in [0, n_src_rows)
+ *   k_new/v_new device [n_src_rows, Hkv, d] pool dtype, 16-byte aligned
+ *   ws          device, at least 16 * row_offsets[n_seqs] bytes, 16-byte
+ *               aligned, not in use by a call still running
+ * Blocks for every sequence are reserved before anything changes, so on
+ * PADOC_ERR_OOM (or any validation error) the pool is as it was.  A forked
+ * sequence's own tokens never go into a block it shares with its parent.
+ * The row list is copied into ws and one scatter kernel runs on stream. */
+PADOC_API int padoc_kv_commit(padoc_kv_pool* pool, int32_t n_seqs, const int32_t* seqs,
+                              const int32_t* row_offsets, const int32_t* rows, int32_t n_src_rows,
+                              const void* k_new, const void* v_new, void* ws, size_t ws_bytes,
+                              padoc_stream_t stream);
+
 /* Critical-path depths of one page (PaDoc, theoretical speedup):
  * d_seq = l(B_1:N) + sum_k l(Y_k);  d_tree = max_k [l(B<=k) + l(Y_k)]. */
 PADOC_API int padoc_depths(const int32_t* layout_len, const int32_t* content_len, int32_t n_regions,

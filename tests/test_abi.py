@@ -179,3 +179,45 @@ def test_pool_rejects_bad_arguments(padoc_lib):
         pool.alloc(33)  # 3 blocks > max_blocks_per_seq
     with pytest.raises(padoc.PadocError):
         pool.seq_info(5)
+
+
+FAKE = 1 << 20  # a pointer value nothing dereferences: every call below fails host checks first
+
+
+def test_commit_rejects_bad_lists_and_oom_changes_nothing(padoc_lib):
+    pool = padoc.KVPool(FAKE, FAKE, 4, Hkv=2, d=128, max_seqs=4, max_blocks_per_seq=8)
+    a, b = pool.alloc(0), pool.alloc(0)
+    s0 = (pool.stats(), pool.seq_info(a), pool.seq_info(b))
+    dev = dict(n_src_rows=40, k_new=FAKE, v_new=FAKE, ws=FAKE, ws_bytes=1 << 20)
+    for seqs, offs, rows in [([a, a], [0, 1, 2], [0, 1]),    # listed twice
+                             ([a, 3], [0, 1, 2], [0, 1]),    # not live
+                             ([a], [0, 2], [0, 40]),         # row out of range
+                             ([a], [1, 2], [0]),             # row_offsets[0] != 0
+                             ([a, b], [0, 2, 1], [0, 1])]:   # decreasing offsets
+        with pytest.raises(padoc.PadocError) as e:
+            pool.commit(seqs, offs, rows, **dev)
+        assert e.value.code == padoc.ERR_INVALID
+    with pytest.raises(padoc.PadocError) as e:  # 3 + 2 blocks wanted, 4 free
+        pool.commit([a, b], [0, 40, 60], list(range(40)) + list(range(20)), **dev)
+    assert e.value.code == padoc.ERR_OOM
+    with pytest.raises(padoc.PadocError) as e:  # workspace below 16 bytes per row
+        pool.commit([a], [0, 2], [0, 1], n_src_rows=40, k_new=FAKE, v_new=FAKE, ws=FAKE, ws_bytes=16)
+    assert e.value.code == padoc.ERR_INVALID
+    with pytest.raises(padoc.PadocError):  # beyond max_blocks_per_seq
+        pool.commit([a], [0, 140], list(range(140)), n_src_rows=140, k_new=FAKE, v_new=FAKE, ws=FAKE,
+                    ws_bytes=1 << 20)
+    assert (pool.stats(), pool.seq_info(a), pool.seq_info(b)) == s0
+    pool.commit([a, b], [0, 0, 0], [], **dev)  # nothing to commit: no device work
+
+
+def test_verify_accept_host_checks(padoc_lib):
+    base = dict(logits=FAKE, nq=4, vocab=10, tokens=FAKE, parents=FAKE, q_offsets=FAKE, n_branches=1,
+                n_acc=FAKE, path=FAKE, free_token=FAKE)
+    for bad in (dict(max_nodes=0, tau=0.75), dict(max_nodes=17, tau=0.75), dict(max_nodes=4, tau=0.0),
+                dict(max_nodes=4, tau=-1.0), dict(max_nodes=4, tau=float("nan")), dict(max_nodes=4, tau=float("inf")),
+                dict(max_nodes=4, tau=0.75, vocab=0), dict(max_nodes=4, tau=0.75, q_offsets=None),
+                dict(max_nodes=4, tau=0.75, path=None), dict(max_nodes=4, tau=0.75, n_branches=-1)):
+        with pytest.raises(padoc.PadocError) as e:
+            padoc.verify_accept(**{**base, **bad})
+        assert e.value.code == padoc.ERR_INVALID
+    padoc.verify_accept(**{**base, "n_branches": 0}, max_nodes=4, tau=0.75)  # nothing to do

@@ -698,6 +698,83 @@ extern "C" int padoc_kv_append(padoc_kv_pool* pool, int32_t seq, const void* k, 
   return PADOC_OK;
 }
 
+extern "C" int padoc_kv_commit(padoc_kv_pool* pool, int32_t n_seqs, const int32_t* seqs, const int32_t* row_offsets,
+                               const int32_t* rows, int32_t n_src_rows, const void* k_new, const void* v_new,
+                               void* ws, size_t ws_bytes, padoc_stream_t stream) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_commit: null pool");
+  if (n_seqs < 0) return fail(PADOC_ERR_INVALID, "kv_commit: n_seqs < 0");
+  if (n_seqs == 0) return PADOC_OK;
+  if (!seqs || !row_offsets) return fail(PADOC_ERR_INVALID, "kv_commit: null seqs / row_offsets");
+  if (row_offsets[0] != 0) return fail(PADOC_ERR_INVALID, "kv_commit: row_offsets[0] must be 0");
+  for (int32_t i = 0; i < n_seqs; ++i)
+    if (row_offsets[i + 1] < row_offsets[i]) return fail(PADOC_ERR_INVALID, "kv_commit: row_offsets decrease at %d", i);
+  const int64_t total = row_offsets[n_seqs];
+  if (total > 0 && !rows) return fail(PADOC_ERR_INVALID, "kv_commit: null rows");
+  for (int64_t j = 0; j < total; ++j)
+    if (rows[j] < 0 || rows[j] >= n_src_rows)
+      return fail(PADOC_ERR_INVALID, "kv_commit: rows[%lld] = %d outside [0, %d)", static_cast<long long>(j), rows[j],
+                  n_src_rows);
+  std::vector<int64_t> extra(n_seqs, 0);
+  int64_t extra_total = 0;
+  PADOC_TRY({
+    std::vector<uint8_t> seen(pool->max_seqs, 0);
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      const int32_t q = seqs[i];
+      if (!pool->seq_ok(q)) return fail(PADOC_ERR_INVALID, "kv_commit: %d is not a live sequence", q);
+      if (seen[q]) return fail(PADOC_ERR_INVALID, "kv_commit: sequence %d listed twice", q);
+      seen[q] = 1;
+      const Seq& s = pool->seqs[q];
+      const int64_t need = (static_cast<int64_t>(s.len - s.fork_len) + row_offsets[i + 1] - row_offsets[i] + pool->bs - 1) /
+                           pool->bs;
+      if (s.n_shared + need > pool->max_bps)
+        return fail(PADOC_ERR_INVALID, "kv_commit: sequence %d would exceed max_blocks_per_seq", q);
+      extra[i] = std::max<int64_t>(0, need - pool->own_blocks(s));
+      extra_total += extra[i];
+    }
+  });
+  if (total == 0) return PADOC_OK;
+  if (!pool->k || !pool->v) return fail(PADOC_ERR_INVALID, "kv_commit: pool has no storage");
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+    return fail(PADOC_ERR_INVALID, "kv_commit: k_new/v_new must be 16-byte aligned device pointers");
+  if (!ws || !aligned16(ws) || ws_bytes < static_cast<size_t>(total) * 16)
+    return fail(PADOC_ERR_INVALID, "kv_commit: ws must be 16-byte aligned and hold %lld bytes",
+                static_cast<long long>(total) * 16);
+  std::vector<int32_t> plan;
+  PADOC_TRY({
+    std::vector<int32_t> fresh;
+    if (extra_total > 0 && (extra_total > static_cast<int64_t>(pool->free_blocks.size()) ||
+                            !pool->take_blocks(static_cast<int32_t>(extra_total), &fresh)))
+      return fail(PADOC_ERR_OOM, "kv_commit: out of blocks (%lld wanted)", static_cast<long long>(extra_total));
+    plan.resize(static_cast<size_t>(total) * 4, 0);
+    size_t next = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      Seq& s = pool->seqs[seqs[i]];
+      s.blocks.insert(s.blocks.end(), fresh.begin() + next, fresh.begin() + next + extra[i]);
+      next += extra[i];
+      const int32_t own = s.len - s.fork_len;
+      for (int32_t j = row_offsets[i]; j < row_offsets[i + 1]; ++j) {
+        const int32_t t = own + (j - row_offsets[i]);
+        int32_t* e = &plan[static_cast<size_t>(j) * 4];
+        e[0] = rows[j];
+        e[1] = s.blocks[s.n_shared + t / pool->bs];
+        e[2] = t % pool->bs;
+      }
+      s.len += row_offsets[i + 1] - row_offsets[i];
+      pool->mark(seqs[i]);
+    }
+  });
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int rc = pool_sync(pool, st);
+  if (rc) return rc;
+  // Pageable source: the call returns once the bytes are staged, so plan may go.
+  const cudaError_t e = cudaMemcpyAsync(ws, plan.data(), plan.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_commit: row list upload");
+  std::string err;
+  rc = launch_commit(pool->k, pool->v, ws, total, pool->Hkv, k_new, v_new, st, &err);
+  if (rc) return fail(rc, "kv_commit: %s", err.c_str());
+  return PADOC_OK;
+}
+
 // ============================================================== decode planning
 
 namespace {
@@ -998,6 +1075,25 @@ namespace padoc {
 int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
 bool pool_has_device_table(const padoc_kv_pool* pool) { return pool && pool->d_table; }
 }  // namespace padoc
+
+extern "C" int padoc_verify_accept(const void* logits, int32_t nq, int32_t vocab, const int32_t* tokens,
+                                   const int32_t* parents, const int32_t* q_offsets, int32_t n_branches,
+                                   int32_t max_nodes, float tau, int32_t* n_acc, int32_t* path, int32_t* free_token,
+                                   padoc_stream_t stream) {
+  if (n_branches < 0 || nq < 0 || vocab <= 0)
+    return fail(PADOC_ERR_INVALID, "verify_accept: n_branches %d, nq %d, vocab %d", n_branches, nq, vocab);
+  if (max_nodes < 1 || max_nodes > 16) return fail(PADOC_ERR_INVALID, "verify_accept: max_nodes %d outside [1, 16]", max_nodes);
+  if (!(tau > 0.f) || !std::isfinite(tau)) return fail(PADOC_ERR_INVALID, "verify_accept: tau must be finite and > 0");
+  if (n_branches == 0) return PADOC_OK;
+  if (!q_offsets || !n_acc || !path || !free_token || (nq > 0 && (!logits || !tokens || !parents)))
+    return fail(PADOC_ERR_INVALID, "verify_accept: null argument");
+  std::string err;
+  const int rc = launch_accept(logits, vocab, nq, tokens, parents, q_offsets, n_branches, max_nodes,
+                               static_cast<float>(std::log(static_cast<double>(tau))), n_acc, path, free_token,
+                               reinterpret_cast<cudaStream_t>(stream), &err);
+  if (rc) return fail(rc, "verify_accept: %s", err.c_str());
+  return PADOC_OK;
+}
 
 // ============================================================== small host helpers
 

@@ -107,6 +107,13 @@ int launch_kv_append(void* k_pool, void* v_pool, const int32_t* table_row, int32
                      int32_t n, int32_t Hkv, int32_t d, const void* k, const void* v,
                      cudaStream_t s, std::string* err);
 
+int launch_accept(const void* logits, int64_t V, int32_t nq, const int32_t* tokens, const int32_t* parents,
+                  const int32_t* q_offsets, int32_t n_branches, int32_t max_nodes, float log_tau,
+                  int32_t* n_acc, int32_t* path, int32_t* free_token, cudaStream_t s, std::string* err);
+// plan: device int4 per row {source row, block, slot, 0}
+int launch_commit(void* k_pool, void* v_pool, const void* plan, int64_t n_rows, int32_t Hkv, const void* k,
+                  const void* v, cudaStream_t s, std::string* err);
+
 // Device error words (set by kernels that give up a bounded wait).
 int read_and_clear_tc_error(cudaStream_t s, unsigned* word);
 

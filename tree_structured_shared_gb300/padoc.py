@@ -29,6 +29,7 @@ EXPORTED = [
     "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
     "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_upload",
     "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free", "padoc_branch_decode_noalloc",
+    "padoc_verify_accept", "padoc_kv_commit",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -97,6 +98,8 @@ def lib() -> C.CDLL:
             "padoc_decode_plan_free": (C.c_int, [vp]),
             "padoc_branch_decode_noalloc": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, vp, vp, vp, vp, vp, vp, f32,
                                                       vp]),
+            "padoc_verify_accept": (C.c_int, [vp, i32, i32, vp, vp, vp, i32, i32, f32, vp, vp, vp, vp]),
+            "padoc_kv_commit": (C.c_int, [vp, i32, p32, p32, p32, i32, vp, vp, vp, C.c_size_t, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -250,6 +253,15 @@ class KVPool:
     def sync(self, stream=None):
         _check(lib().padoc_kv_pool_sync(self.handle, _stream(stream)))
 
+    def commit(self, seqs: Sequence[int], row_offsets: Sequence[int], rows: Sequence[int], n_src_rows: int,
+               k_new, v_new, ws, ws_bytes: int, stream=None):
+        """padoc_kv_commit: appends rows[row_offsets[i]:row_offsets[i+1]] of
+        k_new / v_new to sequence seqs[i]."""
+        a, b, c = _i32(seqs if len(seqs) else [0]), _i32(row_offsets if len(row_offsets) else [0]), \
+            _i32(rows if len(rows) else [0])
+        _check(lib().padoc_kv_commit(self.handle, len(seqs), _p32(a), _p32(b), _p32(c), n_src_rows, _ptr(k_new),
+                                     _ptr(v_new), _ptr(ws), int(ws_bytes), _stream(stream)))
+
     def destroy(self):
         if self.handle:
             lib().padoc_kv_pool_destroy(self.handle)
@@ -293,6 +305,15 @@ def branch_decode_noalloc(pool: KVPool, batch: Batch, Hq: int, q, k_new, v_new, 
     device array (no device allocation; for callers that may not allocate)."""
     _check(lib().padoc_branch_decode_noalloc(pool.handle, C.byref(batch.c), Hq, _ptr(q), _ptr(k_new), _ptr(v_new),
                                              _ptr(tree_bits), _ptr(o), _ptr(lse), float(scale), _stream(stream)))
+
+
+def verify_accept(logits, nq: int, vocab: int, tokens, parents, q_offsets, n_branches: int, max_nodes: int,
+                  tau: float, n_acc, path, free_token, stream=None):
+    """padoc_verify_accept: device arrays in, device n_acc [B], path [B, 16]
+    and free_token [B] out."""
+    _check(lib().padoc_verify_accept(_ptr(logits), nq, vocab, _ptr(tokens), _ptr(parents), _ptr(q_offsets),
+                                     n_branches, max_nodes, float(tau), _ptr(n_acc), _ptr(path), _ptr(free_token),
+                                     _stream(stream)))
 
 
 class DecodePlan:

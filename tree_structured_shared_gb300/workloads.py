@@ -383,3 +383,95 @@ def flatten_branches(w: DecodeWorkload):
             parents.extend(pg.parents[j])
     return (np.asarray(page, np.int32), np.asarray(bpl, np.int32), np.asarray(own, np.int32),
             np.asarray(qoff, np.int32), np.asarray(parents, np.int32))
+
+
+# ----------------------------------------------------------------------------
+# Accept step: draft tokens and next-token logits
+# ----------------------------------------------------------------------------
+
+# The pages name the decoder (HPD-Parsing's InternVL3.5-1B builds on
+# Qwen3-0.6B) but not its vocabulary; this is the size of that model's
+# published embedding table.
+VOCAB = 151936
+
+
+@dataclasses.dataclass
+class AcceptInputs:
+    logits: np.ndarray     # [nq, V] float32 holding bf16 values
+    tokens: np.ndarray     # [nq] int32, the drafted token of each node
+    parents: np.ndarray    # [nq] int32, parent node index within the branch (-1 for node 0)
+    q_offsets: np.ndarray  # [B + 1] int32
+
+
+def _agree_plan(rng: np.random.Generator, parents: np.ndarray, q_offsets: np.ndarray, p_agree: float):
+    """Rows and boost flags for the drafter's agreement with the target: node
+    c of branch b (c >= 1) is 'agreeing' with probability p_agree, and then
+    its parent's row is raised at c's token."""
+    nq = int(q_offsets[-1])
+    base = np.repeat(q_offsets[:-1], np.diff(q_offsets)).astype(np.int64)
+    has_parent = parents >= 0
+    agree = has_parent & (rng.random(nq) < p_agree)
+    parent_row = base + np.where(has_parent, parents, 0)
+    return agree, parent_row
+
+
+def accept_inputs(seed: int, parents_per_branch: Sequence[Sequence[int]], vocab: int, p_agree: float = 0.6,
+                  boost: tuple = (3.5, 5.5), ties: bool = False) -> AcceptInputs:
+    """Host inputs for the accept step.
+
+    Logits are i.i.d. N(0, 1) rounded to bf16 (ties=True: small integers in
+    [-3, 3], so equal scores are common).  Draft tokens are uniform over the
+    vocabulary; each draft node then agrees with the target with probability
+    p_agree, which sets its token's logit in its parent's row to U[boost]
+    (ties=True: to 3 or 4).  That mimics a drafter that is often right, so
+    accepted paths of every length occur."""
+    rng = np.random.default_rng(seed)
+    q_offsets = np.zeros(len(parents_per_branch) + 1, np.int32)
+    q_offsets[1:] = np.cumsum([len(p) for p in parents_per_branch])
+    parents = np.asarray([x for p in parents_per_branch for x in p], np.int32)
+    nq = int(q_offsets[-1])
+    if ties:
+        logits = rng.integers(-3, 4, size=(nq, vocab)).astype(np.float32)
+    else:
+        logits = round_bf16(rng.standard_normal(size=(nq, vocab), dtype=np.float32))
+    tokens = rng.integers(0, vocab, size=nq).astype(np.int32)
+    agree, parent_row = _agree_plan(rng, parents, q_offsets, p_agree)
+    if ties:
+        val = rng.integers(3, 5, size=nq).astype(np.float32)
+    else:
+        val = round_bf16(rng.uniform(boost[0], boost[1], size=nq).astype(np.float32))
+    idx = np.nonzero(agree)[0]
+    logits[parent_row[idx], tokens[idx]] = val[idx]
+    return AcceptInputs(logits, tokens, parents, q_offsets)
+
+
+class DeviceAcceptInputs:
+    """The same recipe drawn on the GPU (torch's seeded CUDA generator) for
+    sizes the host would take long to fill: logits [nq, V] bf16 in HBM."""
+
+    def __init__(self, seed: int, parents_per_branch: Sequence[Sequence[int]], vocab: int, device,
+                 p_agree: float = 0.6, boost: tuple = (3.5, 5.5)):
+        import torch
+        rng = np.random.default_rng(seed)
+        q_offsets = np.zeros(len(parents_per_branch) + 1, np.int32)
+        q_offsets[1:] = np.cumsum([len(p) for p in parents_per_branch])
+        parents = np.asarray([x for p in parents_per_branch for x in p], np.int32)
+        nq = int(q_offsets[-1])
+        tokens = rng.integers(0, vocab, size=nq).astype(np.int32)
+        agree, parent_row = _agree_plan(rng, parents, q_offsets, p_agree)
+        val = round_bf16(rng.uniform(boost[0], boost[1], size=nq).astype(np.float32))
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.logits = torch.randn((nq, vocab), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+        idx = np.nonzero(agree)[0]
+        if len(idx):
+            r = torch.from_numpy(parent_row[idx]).to(device)
+            c = torch.from_numpy(tokens[idx].astype(np.int64)).to(device)
+            self.logits[r, c] = torch.from_numpy(val[idx]).to(device).to(torch.bfloat16)
+        self.tokens, self.parents, self.q_offsets, self.nq, self.vocab = tokens, parents, q_offsets, nq, vocab
+
+    def host_rows(self, rows) -> np.ndarray:
+        """float32 copy of the given logit rows (bf16-exact)."""
+        import torch
+        idx = torch.as_tensor(np.asarray(rows, np.int64), device=self.logits.device)
+        return self.logits.index_select(0, idx).float().cpu().numpy()
