@@ -159,7 +159,7 @@ def test_accept_full_vocab_verify_batch(padoc_lib):
         p, f = acc.accept_tree(rows, inp.tokens[qo[b]:qo[b + 1]], inp.parents[qo[b]:qo[b + 1]], 0.75)
         assert n_acc[b] == len(p) and path[b, :len(p)].tolist() == p and (path[b, len(p):] == -1).all(), b
         assert free[b] == f, b
-    assert n_acc.mean() > 1.0
+    assert n_acc.max() >= 3  # the recipe yields multi-token accepts
 
 
 # ---------------------------------------------------------------------------- commit

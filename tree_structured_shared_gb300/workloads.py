@@ -415,8 +415,8 @@ def _agree_plan(rng: np.random.Generator, parents: np.ndarray, q_offsets: np.nda
     return agree, parent_row
 
 
-def accept_inputs(seed: int, parents_per_branch: Sequence[Sequence[int]], vocab: int, p_agree: float = 0.6,
-                  boost: tuple = (3.5, 5.5), ties: bool = False) -> AcceptInputs:
+def accept_inputs(seed: int, parents_per_branch: Sequence[Sequence[int]], vocab: int, p_agree: float = 0.8,
+                  boost: tuple = (4.0, 6.0), ties: bool = False) -> AcceptInputs:
     """Host inputs for the accept step.
 
     Logits are i.i.d. N(0, 1) rounded to bf16 (ties=True: small integers in
@@ -450,7 +450,7 @@ class DeviceAcceptInputs:
     sizes the host would take long to fill: logits [nq, V] bf16 in HBM."""
 
     def __init__(self, seed: int, parents_per_branch: Sequence[Sequence[int]], vocab: int, device,
-                 p_agree: float = 0.6, boost: tuple = (3.5, 5.5)):
+                 p_agree: float = 0.8, boost: tuple = (4.0, 6.0)):
         import torch
         rng = np.random.default_rng(seed)
         q_offsets = np.zeros(len(parents_per_branch) + 1, np.int32)
