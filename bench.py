@@ -238,6 +238,7 @@ def main() -> int:
     ap.add_argument("--workload", default="serving", choices=sorted(WORKLOADS),
                     help="serving (the default bench line); branch and verify are smaller cases for profiling")
     ap.add_argument("--fwd-seqs", type=int, default=8, help="packed 16384-token sequences in the forward")
+    ap.add_argument("--vocab", type=int, default=151936, help="vocabulary of the verify workload's accept step")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -269,15 +270,26 @@ def main() -> int:
     fwd = harness.Forward(fw, seed=seed)
     dec.plan()
     stream = torch.cuda.current_stream()
+    acc = None
+    if args.workload == "verify":
+        # the accept step over next-token logits of every draft node
+        trees = [t for pg in dw.pages for t in pg.parents]
+        acc = harness.Accept(trees, args.vocab, seed)
+
+    def accept_step():
+        if acc is not None:
+            acc.run()
+
     for _ in range(args.warmup):
         dec.prefix_pass()
         dec.own_pass()
+        accept_step()
         fwd.run()
     torch.cuda.synchronize()
     padoc.device_status()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.2)
@@ -290,8 +302,10 @@ def main() -> int:
         ev[s][1].record(stream)
         dec.own_pass()
         ev[s][2].record(stream)
-        fwd.run()
+        accept_step()
         ev[s][3].record(stream)
+        fwd.run()
+        ev[s][4].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -299,12 +313,13 @@ def main() -> int:
     padoc.device_status()
     t_pre = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     t_own = sum(e[1].elapsed_time(e[2]) for e in ev) / K
-    t_fwd = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    t_acc = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    t_fwd = sum(e[3].elapsed_time(e[4]) for e in ev) / K
     t_dec = t_pre + t_own
-    times = torch.tensor([t_dec, t_fwd, t_pre, t_own], dtype=torch.float64, device="cuda")
+    times = torch.tensor([t_dec, t_fwd, t_pre, t_own, t_acc], dtype=torch.float64, device="cuda")
     if world > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_dec, t_fwd, t_pre, t_own = [float(x) for x in times.tolist()]
+    t_dec, t_fwd, t_pre, t_own, t_acc = [float(x) for x in times.tolist()]
 
     # end to end through the all-in-one C-ABI call, inputs from pinned host memory
     e2e = None
@@ -396,9 +411,17 @@ def main() -> int:
                     "peak": tf_sus, "peak_kind": "bf16 sustained " + peak_src, "frac": fwd_tf / tf_sus,
                     "frac_spec_2250": fwd_tf / 2250.0, "algorithmic_flops": fl,
                     "traffic": traffic_for("forward", fw.n_tokens)},
-        "gpu_launches": 3 * K,
+        "gpu_launches": (5 if acc is not None else 3) * K,
         "clocks": clk,
     }
+    if acc is not None:
+        acc_gbs = acc.bytes / (t_acc * 1e-3) / 1e9
+        line["kernels"]["accept"] = {
+            "ms": t_acc, "achieved_gbs": acc_gbs, "frac_hbm": acc_gbs / hbm, "algorithmic_bytes": acc.bytes,
+            "traffic": traffic_for("accept", acc.nq * args.vocab),
+            "vocab": args.vocab, "draft_nodes": acc.nq, "mean_accepted": acc.mean_accepted(),
+            "what": "row argmax over every draft node's logits + greedy tree walk (tau 0.75)"}
+        line["kernels"]["verify_step"] = {"ms": t_dec + t_acc, "tokens_per_s": nq * world / ((t_dec + t_acc) * 1e-3)}
     if e2e:
         line["e2e"] = e2e
     if cpu:

@@ -219,3 +219,31 @@ class Decode:
         return {"prefix_k": pk.float().cpu().numpy(), "prefix_v": pv.float().cpu().numpy(),
                 "own_k": [o[0].float().cpu().numpy() for o in own],
                 "own_v": [o[1].float().cpu().numpy() for o in own]}
+
+
+class Accept:
+    """The accept step of a verify batch: next-token logits of every draft
+    node resident in HBM (bf16 [nq, vocab]), draft tokens and parents, and
+    the outputs."""
+
+    def __init__(self, trees, vocab: int, seed: int = 0, tau: float = 0.75, device="cuda"):
+        self.inp = wl.DeviceAcceptInputs(seed, trees, vocab, device)
+        self.nq, self.vocab, self.tau = self.inp.nq, vocab, tau
+        self.B = len(trees)
+        self.max_nodes = max(len(t) for t in trees)
+        self.tokens = torch.from_numpy(self.inp.tokens).to(device)
+        self.parents = torch.from_numpy(self.inp.parents).to(device)
+        self.q_offsets = torch.from_numpy(self.inp.q_offsets).to(device)
+        self.n_acc = torch.empty(self.B, dtype=torch.int32, device=device)
+        self.path = torch.empty(self.B, 16, dtype=torch.int32, device=device)
+        self.free = torch.empty(self.B, dtype=torch.int32, device=device)
+        # algorithmic bytes: every logit once, plus the small per-node and per-branch arrays
+        self.bytes = self.nq * vocab * 2 + self.nq * 8 + (self.B + 1) * 4 + self.B * (16 + 2) * 4
+
+    def run(self, stream=None):
+        padoc.verify_accept(self.inp.logits, self.nq, self.vocab, self.tokens, self.parents, self.q_offsets,
+                            self.B, self.max_nodes, self.tau, self.n_acc, self.path, self.free, stream)
+        return self.n_acc, self.path, self.free
+
+    def mean_accepted(self) -> float:
+        return float(self.n_acc.float().mean().item())
