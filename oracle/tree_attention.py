@@ -8,15 +8,15 @@ Readings of the pages that this file fixes (each one also listed in the design
 notes of the repository):
 
 1. The prefix X is the front of the one causal layout stream, so a token of X
-   sees X up to and including itself (PaDoc, "Training paradigm": "the layout
-   stream forms one causal sequence").
+   sees X up to and including itself (PaDoc, "Training paradigm": the whole
+   layout stream is a single causal sequence).
 2. Every query sees itself (standard next-token attention; PaDoc, "Training
    paradigm", teacher-forced next-token objective).
 3. A layout token of B_k sees X, B_1..B_{k-1} and the tokens of B_k up to
    itself (Anc(B_k) = {X, B<k} plus causal order inside B_k).
 4. A content token of Y_k sees X, B_1..B_k and the tokens of Y_k up to itself
-   (Anc(Y_k) = {X, B<=k}; "the query tokens of content branch Yk attend to
-   the virtual key/value sequence [X, B<=k, Yk]").  The branch-start token is
+   (Anc(Y_k) = {X, B<=k}; a query of Y_k reads the keys and values of X,
+   B<=k and Y_k as if they were one sequence).  The branch-start token is
    simply the first token of Y_k.
 5. Pages never see each other, whatever their packing.
 6. scale = 1/sqrt(d); LSE is the natural log of sum(exp(scale * q.k)).

@@ -9,8 +9,8 @@
 //                segment; key tiles walk that segment's key segments (the
 //                ancestors X, B<=k and the causal own segment).  Tiles of
 //                non-ancestor keys are never listed, so they cost nothing.
-//                (PaDoc, "Training paradigm": Y_k queries attend to the
-//                virtual key/value sequence [X, B<=k, Y_k].)
+//                (PaDoc, "Training paradigm": a query of Y_k reads the keys
+//                of X, B<=k and Y_k as if they were one sequence.)
 //   MODE_PREFIX  cascade prefix pass of branch decode.  Rows are the query
 //                rows of every branch of one page; key tiles are one chunk of
 //                the page's shared prefix blocks, read from HBM once for all
