@@ -17,9 +17,13 @@ What it computes, each function citing the passage it follows:
   batching": each draft token sees the accepted sequence and its own
   ancestor path);
 * the log-sum-exp merge of partial softmaxes;
-* the critical-path depths D_seq and D_PaDoc (PaDoc, theoretical speedup).
+* the critical-path depths D_seq and D_PaDoc (PaDoc, theoretical speedup);
+* the accept step of speculative verify (accept.py: HSD page, greedy tree
+  traversal; HPD-Parsing, accepted length of a drafted chain);
+* the draft trie of decoupled speculative verification (draft_trie.py: HSD
+  page, draft-target matching and prefix-tree batching).
 
-Pins: every function here is checked in tests/test_oracle.py against facts
+Pins: every function here is checked in tests/test_oracle*.py against facts
 that do not come from this code (brute-force dense masks built from region
 comparisons, plain causal attention for one region, closed forms, isolation
 under perturbation, hand-worked fixtures under tests/golden/).  No function is
