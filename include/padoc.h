@@ -316,6 +316,47 @@ PADOC_API int padoc_kv_commit(padoc_kv_pool* pool, int32_t n_seqs, const int32_t
                               const void* k_new, const void* v_new, void* ws, size_t ws_bytes,
                               padoc_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Draft trie of decoupled speculative verification (HSD page, "decoupled
+ * speculative verification": draft-target matching and prefix-tree batching).
+ *
+ * A draft index holds one request's fixed drafts (they do not change while
+ * the request decodes) and a table of every window of `window` consecutive
+ * draft tokens (n = 3 in the HSD page).  One step's verify block is then:
+ *   node 0 = the last accepted token (the anchor);
+ *   the last `window` accepted tokens are looked up; each occurrence in a
+ *   draft, taken draft by draft and by position, contributes the draft's
+ *   tokens after it, cut to max_depth - 1 tokens;
+ *   the continuations are merged into a prefix tree (one node per distinct
+ *   prefix, siblings with distinct tokens), nodes numbered in creation order
+ *   (every parent before its children); creation stops once max_nodes nodes
+ *   exist.
+ * Fewer accepted tokens than `window`, or no occurrence, give the anchor
+ * alone.  Everything here is host memory and host work. */
+typedef struct padoc_draft_index padoc_draft_index;
+/* tokens: the drafts concatenated; draft d is tokens[draft_offsets[d] ..
+ * draft_offsets[d+1]) (draft_offsets[0] = 0, non-decreasing); window >= 1.
+ * The index copies what it needs. */
+PADOC_API int padoc_draft_index_create(const int32_t* tokens, const int64_t* draft_offsets, int32_t n_drafts,
+                                       int32_t window, padoc_draft_index** out);
+PADOC_API int padoc_draft_index_free(padoc_draft_index* index);
+/* accepted: the accepted tokens so far (n_accepted >= 1; only the last
+ * `window` are read).  tokens / parents: capacity max_nodes (>= 1);
+ * parents[0] = -1.  max_depth >= 1 counts the anchor. */
+PADOC_API int padoc_draft_trie(const padoc_draft_index* index, const int32_t* accepted, int32_t n_accepted,
+                               int32_t max_nodes, int32_t max_depth, int32_t* tokens, int32_t* parents,
+                               int32_t* n_nodes);
+/* A whole verify batch: branch b uses index[b] and
+ * accepted[acc_offsets[b] .. acc_offsets[b+1]) (at least one token).  Writes
+ * the concatenated blocks: tokens and parents (capacity n_branches *
+ * max_nodes, parents relative to the branch), q_offsets [n_branches + 1] and,
+ * when bits is not NULL, the ancestor-or-self rows [nq] that
+ * padoc_branch_decode takes as tree_bits.  max_nodes in [1, 16]. */
+PADOC_API int padoc_draft_trie_batch(const padoc_draft_index* const* index, int32_t n_branches,
+                                     const int32_t* accepted, const int32_t* acc_offsets, int32_t max_nodes,
+                                     int32_t max_depth, int32_t* tokens, int32_t* parents, int32_t* q_offsets,
+                                     uint16_t* bits);
+
 /* Critical-path depths of one page (PaDoc, theoretical speedup):
  * d_seq = l(B_1:N) + sum_k l(Y_k);  d_tree = max_k [l(B<=k) + l(Y_k)]. */
 PADOC_API int padoc_depths(const int32_t* layout_len, const int32_t* content_len, int32_t n_regions,

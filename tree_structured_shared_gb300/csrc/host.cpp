@@ -1072,7 +1072,14 @@ extern "C" int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch
 }
 
 namespace padoc {
-int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+int set_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  return fail(code, "%s", buf);
+}
 bool pool_has_device_table(const padoc_kv_pool* pool) { return pool && pool->d_table; }
 }  // namespace padoc
 

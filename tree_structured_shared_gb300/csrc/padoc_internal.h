@@ -126,7 +126,7 @@ EncodeTiledFn get_encode_fn(std::string* err);
 int num_sms();
 
 // Records an error message for padoc_last_error() and returns code.
-int set_error(int code, const char* msg);
+int set_error(int code, const char* fmt, ...);
 // True once the pool's device block table exists (padoc_kv_pool_sync ran).
 bool pool_has_device_table(const padoc_kv_pool* pool);
 

@@ -29,7 +29,8 @@ EXPORTED = [
     "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
     "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_upload",
     "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free", "padoc_branch_decode_noalloc",
-    "padoc_verify_accept", "padoc_kv_commit",
+    "padoc_verify_accept", "padoc_kv_commit", "padoc_draft_index_create", "padoc_draft_index_free",
+    "padoc_draft_trie", "padoc_draft_trie_batch",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -100,6 +101,11 @@ def lib() -> C.CDLL:
                                                       vp]),
             "padoc_verify_accept": (C.c_int, [vp, i32, i32, vp, vp, vp, i32, i32, f32, vp, vp, vp, vp]),
             "padoc_kv_commit": (C.c_int, [vp, i32, p32, p32, p32, i32, vp, vp, vp, C.c_size_t, vp]),
+            "padoc_draft_index_create": (C.c_int, [p32, p64, i32, i32, C.POINTER(vp)]),
+            "padoc_draft_index_free": (C.c_int, [vp]),
+            "padoc_draft_trie": (C.c_int, [vp, p32, i32, i32, i32, p32, p32, p32]),
+            "padoc_draft_trie_batch": (C.c_int, [C.POINTER(vp), i32, p32, p32, i32, i32, p32, p32, p32,
+                                                 C.POINTER(C.c_uint16)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -314,6 +320,59 @@ def verify_accept(logits, nq: int, vocab: int, tokens, parents, q_offsets, n_bra
     _check(lib().padoc_verify_accept(_ptr(logits), nq, vocab, _ptr(tokens), _ptr(parents), _ptr(q_offsets),
                                      n_branches, max_nodes, float(tau), _ptr(n_acc), _ptr(path), _ptr(free_token),
                                      _stream(stream)))
+
+
+class DraftIndex:
+    """A request's fixed drafts with their window table (padoc_draft_index)."""
+
+    def __init__(self, drafts: Sequence[Sequence[int]], window: int = 3):
+        toks = _i32([t for d in drafts for t in d] or [0])
+        offs = np.zeros(len(drafts) + 1, np.int64)
+        offs[1:] = np.cumsum([len(d) for d in drafts])
+        h = C.c_void_p()
+        _check(lib().padoc_draft_index_create(_p32(toks), offs.ctypes.data_as(C.POINTER(C.c_int64)), len(drafts),
+                                              window, C.byref(h)))
+        self.handle = h
+
+    def trie(self, accepted: Sequence[int], max_nodes: int = 16, max_depth: int = 7):
+        """One step's verify block: (tokens, parents) lists."""
+        acc = _i32(accepted)
+        t = np.zeros(max_nodes, np.int32)
+        p = np.zeros(max_nodes, np.int32)
+        n = C.c_int32()
+        _check(lib().padoc_draft_trie(self.handle, _p32(acc), len(acc), max_nodes, max_depth, _p32(t), _p32(p),
+                                      C.byref(n)))
+        return t[: n.value].tolist(), p[: n.value].tolist()
+
+    def free(self):
+        if self.handle:
+            lib().padoc_draft_index_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def draft_trie_batch(indexes: Sequence[DraftIndex], accepted: Sequence[Sequence[int]], max_nodes: int = 16,
+                     max_depth: int = 7):
+    """padoc_draft_trie_batch: returns tokens [nq], parents [nq], q_offsets
+    [B + 1] and tree bits [nq] (uint16) as numpy arrays."""
+    B = len(indexes)
+    hs = (C.c_void_p * max(B, 1))(*[ix.handle.value for ix in indexes])
+    acc = _i32([t for a in accepted for t in a] or [0])
+    aoff = np.zeros(B + 1, np.int32)
+    aoff[1:] = np.cumsum([len(a) for a in accepted])
+    cap = max(B * max_nodes, 1)
+    t, p = np.zeros(cap, np.int32), np.zeros(cap, np.int32)
+    q = np.zeros(B + 1, np.int32)
+    bits = np.zeros(cap, np.uint16)
+    _check(lib().padoc_draft_trie_batch(hs, B, _p32(acc), _p32(aoff), max_nodes, max_depth, _p32(t), _p32(p),
+                                        _p32(q), bits.ctypes.data_as(C.POINTER(C.c_uint16))))
+    nq = int(q[-1])
+    return t[:nq], p[:nq], q, bits[:nq]
 
 
 class DecodePlan:

@@ -475,3 +475,30 @@ class DeviceAcceptInputs:
         import torch
         idx = torch.as_tensor(np.asarray(rows, np.int64), device=self.logits.device)
         return self.logits.index_select(0, idx).float().cpu().numpy()
+
+
+def hsd_drafts(seed: int, n_regions: int = 6, region_len: tuple = (20, 120), vocab: int = 151936,
+               p_sub: float = 0.03, p_del: float = 0.02, p_ins: float = 0.02):
+    """A target token sequence and one fixed draft per region, as a parsing
+    pipeline would give (HSD page: region-level drafts with local OCR
+    errors).  Each region of the target is copied into its draft with
+    independent substitutions, deletions and insertions at the given rates.
+    Returns (target, drafts)."""
+    rng = np.random.default_rng(seed)
+    target, drafts = [], []
+    for _ in range(n_regions):
+        region = rng.integers(0, vocab, int(_uniform_int(rng, *region_len))).tolist()
+        target.extend(region)
+        d = []
+        for t in region:
+            u = rng.random()
+            if u < p_del:
+                continue
+            if u < p_del + p_sub:
+                d.append(int(rng.integers(0, vocab)))
+            else:
+                d.append(t)
+            if rng.random() < p_ins:
+                d.append(int(rng.integers(0, vocab)))
+        drafts.append(d)
+    return target, drafts
