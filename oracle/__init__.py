@@ -18,6 +18,8 @@ What it computes, each function citing the passage it follows:
   ancestor path);
 * the log-sum-exp merge of partial softmaxes;
 * the critical-path depths D_seq and D_PaDoc (PaDoc, theoretical speedup);
+* the backward pass of the tree-varlen forward (tree_backward.py: the chain
+  rule through each token's softmax over its ancestor set);
 * the accept step of speculative verify (accept.py: HSD page, greedy tree
   traversal; HPD-Parsing, accepted length of a drafted chain);
 * the draft trie of decoupled speculative verification (draft_trie.py: HSD
