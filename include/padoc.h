@@ -178,6 +178,34 @@ PADOC_API int padoc_kv_pool_stats(const padoc_kv_pool* pool, int32_t* free_block
 PADOC_API int padoc_kv_pool_sync(padoc_kv_pool* pool, padoc_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Backward of the packed tree-varlen forward (training; PaDoc, "Training
+ * paradigm" trains through the same ancestor-masked attention).  For an
+ * upstream gradient dO it returns the gradients of sum(dO * O):
+ *   P = exp(scale q.k - LSE), dP = dO . v, dS = P (dP - rowsum(dO * O)),
+ *   dq = scale sum_j dS k_j,  dk_j = scale sum dS q,  dv_j = sum P dO,
+ * over exactly the (query, ancestor key) pairs of the forward; dk and dv of
+ * a kv head sum over the query heads of its group.
+ *   q, k, v, o, lse  the forward's inputs and outputs (same layouts)
+ *   d_o              device [T, Hq, d], dtype of q
+ *   dq / dk / dv     device, shapes and dtype of q / k / v (overwritten)
+ *   ws               device workspace of padoc_tree_attn_varlen_bwd_ws_size
+ *                    bytes, 256-byte aligned, not in use by a running call
+ * dtype PADOC_BF16 or PADOC_F32; d 64 or 128; Hq / Hkv in {1, 2, 4, 8, 16};
+ * scale as in the forward.  Results are deterministic (no atomics). */
+PADOC_API int padoc_tree_attn_varlen_bwd_ws_size(const padoc_tree_desc* desc, int32_t Hq, size_t* bytes);
+PADOC_API int padoc_tree_attn_varlen_bwd(padoc_tree_desc* desc, const void* q, const void* k, const void* v,
+                                         const void* o, const float* lse, const void* d_o, void* dq, void* dk,
+                                         void* dv, int32_t dtype, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                         void* ws, size_t ws_bytes, padoc_stream_t stream);
+/* The key-stationary half of the backward plan, for checks: items [n][4] =
+ * key tile start, keys in the tile, first entry, entries; entries [m][5] =
+ * keys [k_lo, k_hi), causal, queries [q_lo, q_hi).  Keys of the tile that a
+ * query of an entry sees are those in [k_lo, k_hi), and only j <= t when
+ * causal.  Either output may be NULL. */
+PADOC_API int padoc_tree_desc_bwd_plan(const padoc_tree_desc* desc, int32_t* items, int32_t* entries,
+                                       int64_t* n_items, int64_t* n_entries);
+
+/* ------------------------------------------------------------------------
  * Branch-parallel decode and speculative verify over the pool.
  * Every live branch queries 1..16 tokens against the shared prefix of its
  * page plus its own cached suffix; inside the query block each token sees

@@ -1,7 +1,13 @@
 """Tolerances and comparison helpers for GPU-vs-oracle parity.
 
 bf16 workloads: max-abs error 1.5e-2 and mean-abs error 2e-3 on O; f32
-workloads: max-abs 1e-4 on O; LSE within 1e-3 relative for both."""
+workloads: max-abs 1e-4 on O; LSE within 1e-3 relative for both.
+
+Backward gradients are compared relative to their own scale (their
+magnitudes grow with the number of queries that see a key): bf16 max error
+within 1e-2 of max|ref| and mean error within 5e-3 of mean|ref| (output
+rounding alone is 2^-9 relative; bf16 probabilities in the tensor-core path
+add the same order per term); f32 within 1e-4 and 1e-5."""
 import numpy as np
 
 BF16_MAX_ABS, BF16_MEAN_ABS = 1.5e-2, 2e-3
@@ -25,3 +31,21 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref, dtype="bf16", what=""):
     rel = np.abs(lg - lr) / np.maximum(np.abs(lr), 1e-6)
     assert rel.max() <= LSE_REL, f"{what}: LSE rel {rel.max():.3e}"
     return float(err.max()), float(err.mean()), float(rel.max())
+
+
+GRAD_BF16_MAX, GRAD_BF16_MEAN = 1e-2, 5e-3
+GRAD_F32_MAX, GRAD_F32_MEAN = 1e-4, 1e-5
+
+
+def check_grad(g_gpu, g_ref, dtype="bf16", what=""):
+    g = np.asarray(g_gpu, np.float64)
+    r = np.asarray(g_ref, np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite gradient"
+    err = np.abs(g - r)
+    rmax = err.max() / max(np.abs(r).max(), 1e-30)
+    rmean = err.mean() / max(np.abs(r).mean(), 1e-30)
+    lim = (GRAD_BF16_MAX, GRAD_BF16_MEAN) if dtype == "bf16" else (GRAD_F32_MAX, GRAD_F32_MEAN)
+    assert rmax <= lim[0], f"{what}: max error {rmax:.3e} of max|ref|"
+    assert rmean <= lim[1], f"{what}: mean error {rmean:.3e} of mean|ref|"
+    return float(rmax), float(rmean)

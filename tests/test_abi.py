@@ -221,3 +221,27 @@ def test_verify_accept_host_checks(padoc_lib):
             padoc.verify_accept(**{**base, **bad})
         assert e.value.code == padoc.ERR_INVALID
     padoc.verify_accept(**{**base, "n_branches": 0}, max_nodes=4, tau=0.75)  # nothing to do
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("order", [padoc.PACK_CANONICAL, padoc.PACK_DOCUMENT])
+def test_backward_plan_covers_every_pair_once(padoc_lib, seed, order):
+    """The key-stationary backward entries enumerate exactly the oracle's
+    (query, ancestor) pairs, each once, inside 128-key tiles."""
+    w = wl.random_pages(seed, n_pages=3, max_prefix=300, max_regions=5, max_layout=40, max_content=150)
+    desc = padoc.TreeDesc(w.pages, order)
+    items, entries = desc.bwd_plan()
+    anc = ta.ancestor_positions(w.pages, order)
+    want = np.zeros((w.n_tokens, w.n_tokens), np.int32)
+    for t, a in enumerate(anc):
+        want[t, a] = 1
+    got = np.zeros_like(want)
+    for k_start, k_len, e0, ne in items:
+        assert k_start % 128 == 0 and 0 < k_len <= 128
+        for k_lo, k_hi, causal, q_lo, q_hi in entries[e0:e0 + ne]:
+            assert k_start <= k_lo < k_hi <= k_start + k_len
+            for t in range(q_lo, q_hi):
+                hi = min(k_hi, t + 1) if causal else k_hi
+                if hi > k_lo:
+                    got[t, k_lo:hi] += 1
+    assert np.array_equal(got, want)

@@ -90,6 +90,8 @@ struct DevPlan {
   KVSeg* kvsegs = nullptr;
   FwdItem* items = nullptr;
   int32_t n_items = 0;
+  BwdItem* bitems = nullptr;
+  BwdEntry* bentries = nullptr;
 };
 
 struct padoc_tree_desc {
@@ -97,6 +99,8 @@ struct padoc_tree_desc {
   int64_t pairs = 0;
   std::vector<QSeg> qsegs;
   std::vector<KVSeg> kvsegs;
+  std::vector<BwdItem> bitems;
+  std::vector<BwdEntry> bentries;
   std::vector<DevPlan> dev;
   ~padoc_tree_desc() {
     for (auto& d : dev) {
@@ -106,10 +110,53 @@ struct padoc_tree_desc {
       cudaFree(d.qsegs);
       cudaFree(d.kvsegs);
       cudaFree(d.items);
+      cudaFree(d.bitems);
+      cudaFree(d.bentries);
       if (cur >= 0) cudaSetDevice(cur);
     }
   }
 };
+
+// Transposes the query segments' key lists onto the global key-tile grid
+// (the key-stationary half of the backward); tiles in LPT order by the
+// (query, key) pairs they hold.
+static void build_bwd(padoc_tree_desc* desc) {
+  const int64_t ntiles = (desc->T + kTileKeys - 1) / kTileKeys;
+  std::vector<std::vector<BwdEntry>> per(ntiles);
+  std::vector<int64_t> cost(ntiles, 0);
+  for (const QSeg& s : desc->qsegs) {
+    for (int32_t j = 0; j < s.kv_count; ++j) {
+      const KVSeg& e = desc->kvsegs[s.kv_first + j];
+      if (e.len <= 0) continue;
+      for (int64_t i = e.start / kTileKeys; i <= (static_cast<int64_t>(e.start) + e.len - 1) / kTileKeys; ++i) {
+        BwdEntry b{};
+        b.k_lo = static_cast<int32_t>(std::max<int64_t>(e.start, i * kTileKeys));
+        b.k_hi = static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(e.start) + e.len, (i + 1) * kTileKeys));
+        b.causal = e.causal;
+        b.q_lo = e.causal ? std::max(s.q_start, b.k_lo) : s.q_start;
+        b.q_hi = s.q_start + s.q_len;
+        if (b.q_lo >= b.q_hi) continue;
+        per[i].push_back(b);
+        cost[i] += static_cast<int64_t>(b.q_hi - b.q_lo) * (b.k_hi - b.k_lo);
+      }
+    }
+  }
+  std::vector<int64_t> order;
+  for (int64_t i = 0; i < ntiles; ++i)
+    if (!per[i].empty()) order.push_back(i);
+  std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return cost[a] > cost[b]; });
+  desc->bitems.clear();
+  desc->bentries.clear();
+  for (int64_t i : order) {
+    BwdItem it;
+    it.k_start = static_cast<int32_t>(i * kTileKeys);
+    it.k_len = static_cast<int32_t>(std::min<int64_t>(kTileKeys, desc->T - i * kTileKeys));
+    it.e_first = static_cast<int32_t>(desc->bentries.size());
+    it.e_count = static_cast<int32_t>(per[i].size());
+    desc->bitems.push_back(it);
+    desc->bentries.insert(desc->bentries.end(), per[i].begin(), per[i].end());
+  }
+}
 
 namespace {
 
@@ -244,6 +291,7 @@ extern "C" int padoc_tree_desc_build(const padoc_tree_spec* spec, padoc_tree_des
       }
     }
     desc->pairs = pairs;
+    build_bwd(desc.get());
     d = desc.release();
   });
   *out = d;
@@ -338,10 +386,17 @@ static int upload_desc(padoc_tree_desc* desc, int group, DevPlan** plan_out) {
     e = alloc_copy(reinterpret_cast<void**>(&p.kvsegs), desc->kvsegs.data(), desc->kvsegs.size() * sizeof(KVSeg));
   if (e == cudaSuccess)
     e = alloc_copy(reinterpret_cast<void**>(&p.items), items.data(), items.size() * sizeof(FwdItem));
+  if (e == cudaSuccess)
+    e = alloc_copy(reinterpret_cast<void**>(&p.bitems), desc->bitems.data(), desc->bitems.size() * sizeof(BwdItem));
+  if (e == cudaSuccess)
+    e = alloc_copy(reinterpret_cast<void**>(&p.bentries), desc->bentries.data(),
+                   desc->bentries.size() * sizeof(BwdEntry));
   if (e != cudaSuccess) {
     cudaFree(p.qsegs);
     cudaFree(p.kvsegs);
     cudaFree(p.items);
+    cudaFree(p.bitems);
+    cudaFree(p.bentries);
     return cuda_fail(e, "tree descriptor upload");
   }
   desc->dev.push_back(p);
@@ -398,6 +453,92 @@ extern "C" int padoc_tree_attn_varlen(padoc_tree_desc* desc, const void* q, cons
   rc = dtype == PADOC_BF16 ? launch_fwd_bf16(a, reinterpret_cast<cudaStream_t>(stream), &err)
                            : launch_fwd_f32(a, reinterpret_cast<cudaStream_t>(stream), &err);
   if (rc) return fail(rc, "tree_attn_varlen: %s", err.c_str());
+  return PADOC_OK;
+}
+
+static size_t bwd_ws_bytes(const padoc_tree_desc* desc, int32_t Hq) {
+  return (static_cast<size_t>(Hq) * desc->T * sizeof(float) + 255) / 256 * 256;
+}
+
+extern "C" int padoc_tree_attn_varlen_bwd_ws_size(const padoc_tree_desc* desc, int32_t Hq, size_t* bytes) {
+  if (!desc || !bytes) return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd_ws_size: null argument");
+  if (Hq <= 0) return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd_ws_size: Hq must be positive");
+  *bytes = bwd_ws_bytes(desc, Hq);
+  return PADOC_OK;
+}
+
+extern "C" int padoc_tree_attn_varlen_bwd(padoc_tree_desc* desc, const void* q, const void* k, const void* v,
+                                          const void* o, const float* lse, const void* d_o, void* dq, void* dk,
+                                          void* dv, int32_t dtype, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                          void* ws, size_t ws_bytes, padoc_stream_t stream) {
+  if (!desc) return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd: null descriptor");
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd: Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  const int group = Hq / Hkv;
+  if (!valid_group(group))
+    return fail(PADOC_ERR_UNSUPPORTED, "tree_attn_varlen_bwd: Hq/Hkv=%d not in {1,2,4,8,16}", group);
+  if (dtype != PADOC_BF16 && dtype != PADOC_F32) return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd: unknown dtype %d", dtype);
+  if (d != 64 && d != 128) return fail(PADOC_ERR_UNSUPPORTED, "tree_attn_varlen_bwd: d must be 64 or 128");
+  if (desc->T == 0) return PADOC_OK;
+  if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv)
+    return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd: null tensor");
+  for (const void* p : {q, k, v, o, static_cast<const void*>(lse), d_o, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (!aligned16(p)) return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd: tensors must be 16-byte aligned");
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < bwd_ws_bytes(desc, Hq))
+    return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd: ws must be 256-byte aligned and hold %zu bytes",
+                bwd_ws_bytes(desc, Hq));
+  DevPlan* plan = nullptr;
+  int rc = upload_desc(desc, group, &plan);
+  if (rc) return rc;
+  BwdArgs a;
+  a.fwd = {plan->qsegs, plan->kvsegs, plan->items, plan->n_items, group, plan->tile_tokens};
+  a.bwd = {plan->bitems, plan->bentries, static_cast<int32_t>(desc->bitems.size())};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dout = d_o;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = static_cast<float*>(ws);
+  a.T = desc->T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
+  std::string err;
+  rc = launch_bwd_core(a, dtype, reinterpret_cast<cudaStream_t>(stream), &err);
+  if (rc) return fail(rc, "tree_attn_varlen_bwd: %s", err.c_str());
+  return PADOC_OK;
+}
+
+extern "C" int padoc_tree_desc_bwd_plan(const padoc_tree_desc* desc, int32_t* items, int32_t* entries,
+                                        int64_t* n_items, int64_t* n_entries) {
+  if (!desc) return fail(PADOC_ERR_INVALID, "tree_desc_bwd_plan: null descriptor");
+  if (n_items) *n_items = static_cast<int64_t>(desc->bitems.size());
+  if (n_entries) *n_entries = static_cast<int64_t>(desc->bentries.size());
+  if (items)
+    for (size_t i = 0; i < desc->bitems.size(); ++i) {
+      const BwdItem& it = desc->bitems[i];
+      int32_t* r = items + 4 * i;
+      r[0] = it.k_start;
+      r[1] = it.k_len;
+      r[2] = it.e_first;
+      r[3] = it.e_count;
+    }
+  if (entries)
+    for (size_t i = 0; i < desc->bentries.size(); ++i) {
+      const BwdEntry& b = desc->bentries[i];
+      int32_t* r = entries + 5 * i;
+      r[0] = b.k_lo;
+      r[1] = b.k_hi;
+      r[2] = b.causal;
+      r[3] = b.q_lo;
+      r[4] = b.q_hi;
+    }
   return PADOC_OK;
 }
 

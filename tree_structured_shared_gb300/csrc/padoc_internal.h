@@ -48,6 +48,42 @@ struct FwdArgs {
   float scale;
 };
 
+// ---------------------------------------------------------------- backward
+// Key-stationary work of the backward: keys are cut into tiles on a global
+// kTileKeys grid; an entry lists queries [q_lo, q_hi) of one query segment
+// that see keys [k_lo, k_hi) of the tile through one key segment (when
+// causal, a query at t sees only keys <= t).  Entries of one tile cover
+// disjoint (query, key) pairs, so their contributions simply add.
+struct BwdEntry {
+  int32_t k_lo, k_hi, causal, q_lo, q_hi, pad[3];
+};
+struct BwdItem {
+  int32_t k_start, k_len, e_first, e_count;
+};
+struct BwdPlan {
+  const BwdItem* items;
+  const BwdEntry* entries;
+  int32_t n_items;
+};
+
+struct BwdArgs {
+  FwdPlan fwd;  // query-stationary work (dQ), as in the forward
+  BwdPlan bwd;  // key-stationary work (dK, dV)
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;   // [Hq, T]
+  const void* dout;   // [T, Hq, d]
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;       // workspace [Hq, T]: rowsum(dO * O)
+  int64_t T;
+  int32_t Hq, Hkv, d;
+  float scale;
+};
+
 // ---------------------------------------------------------------- decode
 struct DecPage {
   int32_t seq;           // block-table row holding the shared prefix
@@ -113,6 +149,8 @@ int launch_accept(const void* logits, int64_t V, int32_t nq, const int32_t* toke
 // plan: device int4 per row {source row, block, slot, 0}
 int launch_commit(void* k_pool, void* v_pool, const void* plan, int64_t n_rows, int32_t Hkv, const void* k,
                   const void* v, cudaStream_t s, std::string* err);
+
+int launch_bwd_core(const BwdArgs& a, int32_t dtype, cudaStream_t s, std::string* err);
 
 // Device error words (set by kernels that give up a bounded wait).
 int read_and_clear_tc_error(cudaStream_t s, unsigned* word);

@@ -61,6 +61,42 @@ class Forward:
         return 4.0 * self.w.d * self.w.Hq * self.desc.info()["ancestor_pairs"]
 
 
+class Backward:
+    """The backward of a Forward: upstream gradient dO resident on the GPU,
+    gradients and workspace allocated once."""
+
+    def __init__(self, fwd: Forward, d_o=None, seed: int = 0, device="cuda"):
+        self.f = fwd
+        w = fwd.w
+        tdt = fwd.q.dtype
+        if d_o is None:
+            g = torch.Generator(device=device)
+            g.manual_seed(seed + 77)
+            self.d_o = (torch.randn(fwd.T, w.Hq, w.d, device=device, generator=g) * w.value_scale).to(tdt)
+        elif w.dtype == "bf16":
+            self.d_o = _bf16(d_o, device)
+        else:
+            self.d_o = torch.from_numpy(np.ascontiguousarray(d_o, np.float32)).to(device)
+        self.dq = torch.empty_like(fwd.q)
+        self.dk = torch.empty_like(fwd.k)
+        self.dv = torch.empty_like(fwd.v)
+        self.ws_bytes = padoc.tree_attn_varlen_bwd_ws_size(fwd.desc, w.Hq)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+
+    def run(self, stream=None):
+        f, w = self.f, self.f.w
+        padoc.tree_attn_varlen_bwd(f.desc, f.q, f.k, f.v, f.o, f.lse, self.d_o, self.dq, self.dk, self.dv, f.dtype,
+                                   w.Hq, w.Hkv, w.d, self.ws, self.ws_bytes, 0.0, stream)
+        return self.dq, self.dk, self.dv
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic flops: five products of 2 d flops per (query,
+        ancestor) pair and query head -- q.k (the scores, recomputed),
+        dO.v, dS k, dS q and P dO -- so 10 d, 2.5 times the forward."""
+        return 10.0 * self.f.w.d * self.f.w.Hq * self.f.desc.info()["ancestor_pairs"]
+
+
 # ------------------------------------------------------------------ decode
 
 

@@ -30,7 +30,8 @@ EXPORTED = [
     "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_upload",
     "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free", "padoc_branch_decode_noalloc",
     "padoc_verify_accept", "padoc_kv_commit", "padoc_draft_index_create", "padoc_draft_index_free",
-    "padoc_draft_trie", "padoc_draft_trie_batch",
+    "padoc_draft_trie", "padoc_draft_trie_batch", "padoc_tree_attn_varlen_bwd_ws_size",
+    "padoc_tree_attn_varlen_bwd", "padoc_tree_desc_bwd_plan",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -101,6 +102,10 @@ def lib() -> C.CDLL:
                                                       vp]),
             "padoc_verify_accept": (C.c_int, [vp, i32, i32, vp, vp, vp, i32, i32, f32, vp, vp, vp, vp]),
             "padoc_kv_commit": (C.c_int, [vp, i32, p32, p32, p32, i32, vp, vp, vp, C.c_size_t, vp]),
+            "padoc_tree_attn_varlen_bwd_ws_size": (C.c_int, [vp, i32, C.POINTER(C.c_size_t)]),
+            "padoc_tree_attn_varlen_bwd": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                     f32, vp, C.c_size_t, vp]),
+            "padoc_tree_desc_bwd_plan": (C.c_int, [vp, p32, p32, p64, p64]),
             "padoc_draft_index_create": (C.c_int, [p32, p64, i32, i32, C.POINTER(vp)]),
             "padoc_draft_index_free": (C.c_int, [vp]),
             "padoc_draft_trie": (C.c_int, [vp, p32, i32, i32, i32, p32, p32, p32]),
@@ -182,6 +187,15 @@ class TreeDesc:
         _check(lib().padoc_tree_desc_segments(self.handle, _p32(qs), _p32(kv)))
         return qs[: inf["n_qsegs"]], kv[: inf["n_kvsegs"]]
 
+    def bwd_plan(self):
+        """Key-stationary backward plan: items [n, 4], entries [m, 5]."""
+        n, m = C.c_int64(), C.c_int64()
+        _check(lib().padoc_tree_desc_bwd_plan(self.handle, None, None, C.byref(n), C.byref(m)))
+        it = np.zeros((max(n.value, 1), 4), np.int32)
+        en = np.zeros((max(m.value, 1), 5), np.int32)
+        _check(lib().padoc_tree_desc_bwd_plan(self.handle, _p32(it), _p32(en), None, None))
+        return it[: n.value], en[: m.value]
+
     def upload(self, group: int):
         _check(lib().padoc_tree_desc_upload(self.handle, group))
 
@@ -201,6 +215,19 @@ def tree_attn_varlen(desc: TreeDesc, q, k, v, o, lse, dtype: int, Hq: int, Hkv: 
                      scale: float = 0.0, stream=None):
     _check(lib().padoc_tree_attn_varlen(desc.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), dtype, Hq,
                                         Hkv, d, float(scale), _stream(stream)))
+
+
+def tree_attn_varlen_bwd_ws_size(desc: TreeDesc, Hq: int) -> int:
+    n = C.c_size_t()
+    _check(lib().padoc_tree_attn_varlen_bwd_ws_size(desc.handle, Hq, C.byref(n)))
+    return n.value
+
+
+def tree_attn_varlen_bwd(desc: TreeDesc, q, k, v, o, lse, d_o, dq, dk, dv, dtype: int, Hq: int, Hkv: int, d: int,
+                         ws, ws_bytes: int, scale: float = 0.0, stream=None):
+    _check(lib().padoc_tree_attn_varlen_bwd(desc.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                                            _ptr(dq), _ptr(dk), _ptr(dv), dtype, Hq, Hkv, d, float(scale), _ptr(ws),
+                                            int(ws_bytes), _stream(stream)))
 
 
 # ------------------------------------------------------------------ KV pool
