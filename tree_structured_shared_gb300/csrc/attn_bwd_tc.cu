@@ -1,0 +1,715 @@
+// Tensor-core backward of the tree-varlen forward (tcgen05 + TMEM + TMA).
+//
+// The gradients of sum(dO * O) through each token's softmax over its
+// ancestor set (PaDoc, "Training paradigm": the model trains through the
+// same ancestor-masked attention) are split into two persistent kernels
+// that both recompute the probabilities from the forward's LSE:
+//
+//   bwd_dq_kernel   query-stationary, the forward's work units (128 rows =
+//                   query tokens x heads of one GQA group) and key-tile walk:
+//                     S = Q K^T, dP = dO V^T            (tensor cores)
+//                     dS = P (dP - D), P = exp(S - LSE)  (warps 0-3, row = lane)
+//                     dQ += dS K                         (tensor cores, A = dS in TMEM)
+//   bwd_dkv_kernel  key-stationary over the transposed segment lists: a CTA
+//                   keeps one 128-key tile of K and V and walks the query
+//                   tiles that see it:
+//                     S^T = K Q^T, dP^T = V dO^T         (tensor cores)
+//                     P^T, dS^T                          (warps 0-3, key = lane)
+//                     dV += P^T dO, dK += dS^T Q         (tensor cores, A in TMEM)
+// Neither kernel needs atomics: every output row belongs to one unit.
+//
+// Roles (192 threads): warps 0-3 element-wise work and epilogue, warp 4 TMA
+// producer, warp 5 MMA issuer (one thread).  Every wait is bounded; a timed
+// out wait raises the CTA abort flag and this file's device error word.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <string>
+
+#include "../../include/padoc.h"
+#include "padoc_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace padoc {
+
+__device__ unsigned int g_bwd_err;
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 192;
+constexpr int kHalf = 16384;  // one 64-column half of a 128-row bf16 tile
+constexpr int kTile = 2 * kHalf;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+__device__ __forceinline__ void raise_abort(volatile int* abort, unsigned site) {
+  *abort = 1;
+  atomicOr(&g_bwd_err, site);
+}
+
+struct DqParams {
+  FwdPlan plan;
+  int n_units;
+  int32_t Hq, Hkv, group;
+  int64_t T;
+  float sl2, scale;
+  const float* lse;
+  const float* delta;
+  __nv_bfloat16* dq;
+};
+
+struct DkvParams {
+  BwdPlan plan;
+  int n_units;
+  int32_t Hq, Hkv, group, tile_tokens;
+  int64_t T;
+  float sl2, scale;
+  const float* lse;
+  const float* delta;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+};
+
+// ============================================================ dQ pass
+// smem: Q | dO | K ring (2) | V ring (2) | barriers
+constexpr int Q_SM_Q = 0;
+constexpr int Q_SM_DO = kTile;
+constexpr int Q_SM_K = 2 * kTile;
+constexpr int Q_SM_V = Q_SM_K + 2 * kTile;
+constexpr int Q_SM_BAR = Q_SM_V + 2 * kTile;
+constexpr int kDqSmem = Q_SM_BAR + 256 + 1024;
+// TMEM columns
+constexpr uint32_t Q_T_S = 0, Q_T_DP = 128, Q_T_DS = 256, Q_T_DQ = 384;
+enum {
+  QB_QD_FULL = 0,
+  QB_QD_EMPTY = 1,
+  QB_KV_FULL = 2,   // +stage (2)
+  QB_KV_EMPTY = 4,  // +stage (2)
+  QB_SP_FULL = 6,
+  QB_SPARE = 7,
+  QB_DS_FULL = 8,   // count 4
+  QB_DQ_DONE = 9,
+  QB_ACC_FREE = 10,  // count 4
+  QB_N = 11
+};
+
+struct DqUnit {
+  int32_t g, tile_start, q_end, kv_first, kv_count, tile_last;
+};
+
+__device__ __forceinline__ DqUnit dq_unit(const DqParams& p, int u) {
+  DqUnit w;
+  w.g = u % p.Hkv;
+  const FwdItem it = p.plan.items[u / p.Hkv];
+  const QSeg qs = p.plan.qsegs[it.qseg];
+  w.tile_start = it.tile_start;
+  w.q_end = qs.q_start + qs.q_len;
+  w.kv_first = qs.kv_first;
+  w.kv_count = qs.kv_count;
+  w.tile_last = min(it.tile_start + p.plan.tile_tokens, w.q_end) - 1;
+  return w;
+}
+
+// Key tiles of a dQ unit: each key segment in 128-key steps, causal
+// segments cut after the unit's last query.
+struct KeyIter {
+  int32_t s, ks, end, causal;
+};
+__device__ __forceinline__ bool key_setup(const DqParams& p, const DqUnit& w, KeyIter& t) {
+  while (t.s < w.kv_first + w.kv_count) {
+    const KVSeg kv = p.plan.kvsegs[t.s];
+    int32_t end = kv.start + kv.len;
+    if (kv.causal) end = min(end, w.tile_last + 1);
+    if (end > kv.start) {
+      t.ks = kv.start;
+      t.end = end;
+      t.causal = kv.causal;
+      return true;
+    }
+    ++t.s;
+  }
+  return false;
+}
+__device__ __forceinline__ bool key_begin(const DqParams& p, const DqUnit& w, KeyIter& t) {
+  t.s = w.kv_first;
+  return key_setup(p, w, t);
+}
+__device__ __forceinline__ bool key_next(const DqParams& p, const DqUnit& w, KeyIter& t) {
+  t.ks += kTileKeys;
+  if (t.ks < t.end) return true;
+  ++t.s;
+  return key_setup(p, w, t);
+}
+__device__ __forceinline__ int key_count(const DqParams& p, const DqUnit& w) {
+  int n = 0;
+  KeyIter t;
+  for (bool ok = key_begin(p, w, t); ok; ok = key_next(p, w, t)) ++n;
+  return n;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DqParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Q_SM_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Q_SM_BAR + QB_N * 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + Q_SM_BAR + QB_N * 8 + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < QB_N; ++i)
+      mbar_init(bar(i), (i == QB_DS_FULL || i == QB_ACC_FREE) ? 4u : 1u);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int G = p.group, tt = p.plan.tile_tokens;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t kv_it = 0, unit_it = 0;
+      bool failed = false;
+      for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+        const DqUnit w = dq_unit(p, u);
+        if (key_count(p, w) == 0) continue;
+        if (!mbar_wait(bar(QB_QD_EMPTY), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
+        mbar_arrive_expect_tx(bar(QB_QD_FULL), 2 * kTile);
+        for (int hh = 0; hh < G; ++hh)
+          for (int h = 0; h < 2; ++h) {
+            tma_load_3d(sbase + Q_SM_Q + h * kHalf + hh * tt * 128, &tm_q, bar(QB_QD_FULL), h * 64, w.g * G + hh,
+                        w.tile_start);
+            tma_load_3d(sbase + Q_SM_DO + h * kHalf + hh * tt * 128, &tm_do, bar(QB_QD_FULL), h * 64, w.g * G + hh,
+                        w.tile_start);
+          }
+        KeyIter t;
+        for (bool ok = key_begin(p, w, t); ok; ok = key_next(p, w, t), ++kv_it) {
+          const int st = kv_it & 1;
+          if (!mbar_wait(bar(QB_KV_EMPTY + st), ((kv_it >> 1) & 1) ^ 1, abort)) { failed = true; break; }
+          mbar_arrive_expect_tx(bar(QB_KV_FULL + st), 2 * kTile);
+          for (int h = 0; h < 2; ++h) {
+            tma_load_3d(sbase + Q_SM_K + st * kTile + h * kHalf, &tm_k, bar(QB_KV_FULL + st), h * 64, w.g, t.ks);
+            tma_load_3d(sbase + Q_SM_V + st * kTile + h * kHalf, &tm_v, bar(QB_KV_FULL + st), h * 64, w.g, t.ks);
+          }
+        }
+        ++unit_it;
+      }
+      if (failed) raise_abort(abort, 0x10);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);  // both K-major
+      constexpr uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);   // B MN-major
+      uint32_t kv_it = 0, g_it = 0, unit_it = 0;
+      bool failed = false;
+      auto issue_dq = [&](uint32_t tile_it, bool first) -> bool {
+        // dQ += dS K for tile tile_it (dS in TMEM, K of its stage as MN-major B)
+        if (!mbar_wait_relaxed(bar(QB_DS_FULL), tile_it & 1, abort)) return false;
+        tc_fence_after();
+        const int st = tile_it & 1;
+        const uint32_t ka = sbase + Q_SM_K + st * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + Q_T_DQ, tmem + Q_T_DS + kk * 8, sdesc_sw128(ka + kk * 2048, kHalf, 1024), id_mn,
+                      (!first || kk > 0) ? 1u : 0u);
+        mma_commit(bar(QB_KV_EMPTY + st));
+        mma_commit(bar(QB_DQ_DONE));
+        return true;
+      };
+      for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+        const DqUnit w = dq_unit(p, u);
+        const int n = key_count(p, w);
+        if (n == 0) continue;
+        if (!mbar_wait_relaxed(bar(QB_QD_FULL), unit_it & 1, abort)) { failed = true; break; }
+        const uint32_t qa = sbase + Q_SM_Q, da = sbase + Q_SM_DO;
+        for (int j = 0; j < n; ++j, ++kv_it, ++g_it) {
+          // dQ of the previous tile first: once its dS is in, the S and dP
+          // columns are free too (the element-wise warps read them before)
+          if (j > 0) {
+            if (j == 1 && !mbar_wait_relaxed(bar(QB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
+            if (!issue_dq(g_it - 1, j == 1)) { failed = true; break; }
+          }
+          const int st = kv_it & 1;
+          if (!mbar_wait_relaxed(bar(QB_KV_FULL + st), (kv_it >> 1) & 1, abort)) { failed = true; break; }
+          tc_fence_after();
+          const uint32_t ka = sbase + Q_SM_K + st * kTile, va = sbase + Q_SM_V + st * kTile;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            mma_bf16_ss(tmem + Q_T_S, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), id_kk,
+                        kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            mma_bf16_ss(tmem + Q_T_DP, sdesc_sw128(da + off, 16, 1024), sdesc_sw128(va + off, 16, 1024), id_kk,
+                        kk > 0);
+          }
+          mma_commit(bar(QB_SP_FULL));
+          if (j == n - 1) mma_commit(bar(QB_QD_EMPTY));
+        }
+        if (failed) break;
+        if (n == 1 && !mbar_wait_relaxed(bar(QB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
+        if (!issue_dq(g_it - 1, n == 1)) { failed = true; break; }
+        ++unit_it;
+      }
+      if (failed) raise_abort(abort, 0x20);
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise (warps 0-3)
+    const int r = threadIdx.x;  // query row == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t g_it = 0;
+    bool failed = false;
+    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+      const DqUnit w = dq_unit(p, u);
+      const int n = key_count(p, w);
+      if (n == 0) continue;
+      const int hh = r / tt;
+      const int64_t qpos = w.tile_start + (r % tt);
+      const bool valid = qpos < w.q_end;
+      const int head = w.g * G + hh;
+      const float lse2 = valid ? p.lse[static_cast<int64_t>(head) * p.T + qpos] * kLog2e : INFINITY;
+      const float Dr = valid ? p.delta[static_cast<int64_t>(head) * p.T + qpos] : 0.f;
+      KeyIter t;
+      for (bool ok = key_begin(p, w, t); ok; ok = key_next(p, w, t), ++g_it) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_SP_FULL), g_it & 1, abort))) { failed = true; break; }
+        tc_fence_after();
+        const int32_t klen = min(kTileKeys, t.end - t.ks);
+        int32_t vis = valid ? klen : 0;
+        if (t.causal) vis = min(vis, static_cast<int32_t>(qpos + 1 - t.ks));
+        // dS goes over the previous tile's dS: that tile's dQ completed before
+        // this tile's S (tensor operations complete in issue order)
+        if (g_it > 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_DQ_DONE), (g_it - 1) & 1, abort))) { failed = true; break; }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32], dv[32], pk[16];
+          tmem_ld32(tmem + lb + Q_T_S + c * 32, sv);
+          tmem_ld32(tmem + lb + Q_T_DP + c * 32, dv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int col = c * 32 + i;
+            const float p0 = col < vis ? fast_exp2(fmaf(__uint_as_float(sv[i]), p.sl2, -lse2)) : 0.f;
+            const float p1 = col + 1 < vis ? fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.sl2, -lse2)) : 0.f;
+            pk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[i]) - Dr), p1 * (__uint_as_float(dv[i + 1]) - Dr));
+          }
+          tmem_st16(tmem + lb + Q_T_DS + c * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_DS_FULL));
+      }
+      if (failed) break;
+      // epilogue: dQ of this row
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_DQ_DONE), (g_it - 1) & 1, abort))) { failed = true; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lb + Q_T_DQ + c * 32, v);
+        tmem_wait_ld();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dq + (qpos * p.Hq + head) * kHeadDim + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * p.scale, __uint_as_float(v[8 * i + 1]) * p.scale),
+                                pack_bf16x2(__uint_as_float(v[8 * i + 2]) * p.scale, __uint_as_float(v[8 * i + 3]) * p.scale),
+                                pack_bf16x2(__uint_as_float(v[8 * i + 4]) * p.scale, __uint_as_float(v[8 * i + 5]) * p.scale),
+                                pack_bf16x2(__uint_as_float(v[8 * i + 6]) * p.scale, __uint_as_float(v[8 * i + 7]) * p.scale));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(QB_ACC_FREE));
+    }
+    if (failed && lane == 0) raise_abort(abort, 0x40);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================ dK / dV pass
+// smem: K | V | (Q, dO) ring (2) | row data ring (2 x [lse2 128 | D 128]) | barriers
+constexpr int K_SM_K = 0;
+constexpr int K_SM_V = kTile;
+constexpr int K_SM_QD = 2 * kTile;          // stage s: Q at +s*2*kTile, dO at +kTile
+constexpr int K_SM_ROW = K_SM_QD + 4 * kTile;
+constexpr int K_SM_BAR = K_SM_ROW + 2 * 1024;
+constexpr int kDkvSmem = K_SM_BAR + 256 + 1024;
+constexpr uint32_t K_T_S = 0, K_T_DP = 128, K_T_DV = 256, K_T_DK = 384;
+enum {
+  KB_KV_FULL = 0,
+  KB_KV_EMPTY = 1,
+  KB_QD_FULL = 2,   // +stage (2)
+  KB_QD_EMPTY = 4,  // +stage (2)
+  KB_SP_FULL = 6,
+  KB_PDS_FULL = 7,  // count 4
+  KB_ACC_DONE = 8,
+  KB_ACC_FREE = 9,  // count 4
+  KB_N = 10
+};
+
+// Query tiles of a key tile: each entry's queries in steps of tile_tokens.
+struct QIter {
+  int32_t e, e_end, t0;
+  BwdEntry be;
+};
+__device__ __forceinline__ bool q_begin(const DkvParams& p, const BwdItem& it, QIter& q) {
+  q.e = it.e_first;
+  q.e_end = it.e_first + it.e_count;
+  if (q.e >= q.e_end) return false;
+  q.be = p.plan.entries[q.e];
+  q.t0 = q.be.q_lo;
+  return true;
+}
+__device__ __forceinline__ bool q_next(const DkvParams& p, QIter& q) {
+  q.t0 += p.tile_tokens;
+  if (q.t0 < q.be.q_hi) return true;
+  if (++q.e >= q.e_end) return false;
+  q.be = p.plan.entries[q.e];
+  q.t0 = q.be.q_lo;
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const DkvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K_SM_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K_SM_BAR + KB_N * 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + K_SM_BAR + KB_N * 8 + 4);
+  float* rowdata = reinterpret_cast<float*>(smem + K_SM_ROW);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < KB_N; ++i) mbar_init(bar(i), (i == KB_PDS_FULL || i == KB_ACC_FREE) ? 4u : 1u);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int G = p.group, tt = p.tile_tokens;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    uint32_t qd_it = 0, unit_it = 0;
+    bool failed = false;
+    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+      const BwdItem it = p.plan.items[u / p.Hkv];
+      const int g = u % p.Hkv;
+      QIter q;
+      if (!q_begin(p, it, q)) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_KV_EMPTY), (unit_it & 1) ^ 1, abort))) { failed = true; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(KB_KV_FULL), 2 * kTile);
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(sbase + K_SM_K + h * kHalf, &tm_k, bar(KB_KV_FULL), h * 64, g, it.k_start);
+          tma_load_3d(sbase + K_SM_V + h * kHalf, &tm_v, bar(KB_KV_FULL), h * 64, g, it.k_start);
+        }
+      }
+      for (bool ok = true; ok; ok = q_next(p, q), ++qd_it) {
+        const int st = qd_it & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_QD_EMPTY + st), ((qd_it >> 1) & 1) ^ 1, abort))) {
+          failed = true;
+          break;
+        }
+        // LSE (log2 units) and D of the tile's rows; rows past the entry get
+        // LSE = +inf so that their probabilities vanish
+        float* rd = rowdata + st * 256;
+        for (int c = lane; c < 128; c += 32) {
+          const int64_t tok = q.t0 + (c % tt);
+          const int head = g * G + c / tt;
+          const bool ok2 = tok < q.be.q_hi;
+          rd[c] = ok2 ? p.lse[static_cast<int64_t>(head) * p.T + tok] * kLog2e : INFINITY;
+          rd[128 + c] = ok2 ? p.delta[static_cast<int64_t>(head) * p.T + tok] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(KB_QD_FULL + st), 2 * kTile);
+          const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile;
+          for (int hh = 0; hh < G; ++hh)
+            for (int h = 0; h < 2; ++h) {
+              tma_load_3d(qa + h * kHalf + hh * tt * 128, &tm_q, bar(KB_QD_FULL + st), h * 64, g * G + hh, q.t0);
+              tma_load_3d(qa + kTile + h * kHalf + hh * tt * 128, &tm_do, bar(KB_QD_FULL + st), h * 64, g * G + hh,
+                          q.t0);
+            }
+        }
+      }
+      ++unit_it;
+    }
+    if (failed && lane == 0) raise_abort(abort, 0x100);
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);
+      uint32_t qd_it = 0, g_it = 0, unit_it = 0;
+      bool failed = false;
+      for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+        const BwdItem it = p.plan.items[u / p.Hkv];
+        QIter q;
+        if (!q_begin(p, it, q)) continue;
+        if (!mbar_wait_relaxed(bar(KB_KV_FULL), unit_it & 1, abort)) { failed = true; break; }
+        const uint32_t ka = sbase + K_SM_K, va = sbase + K_SM_V;
+        bool first = true;
+        for (bool ok = true; ok; ok = q_next(p, q), ++qd_it, ++g_it) {
+          const int st = qd_it & 1;
+          if (!mbar_wait_relaxed(bar(KB_QD_FULL + st), (qd_it >> 1) & 1, abort)) { failed = true; break; }
+          tc_fence_after();
+          const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile, da = qa + kTile;
+          // S^T = K Q^T and dP^T = V dO^T; the previous tile's dV / dK MMAs,
+          // which read P^T / dS^T from these columns, were issued earlier
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            mma_bf16_ss(tmem + K_T_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), id_kk,
+                        kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            mma_bf16_ss(tmem + K_T_DP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), id_kk,
+                        kk > 0);
+          }
+          mma_commit(bar(KB_SP_FULL));
+          if (!mbar_wait_relaxed(bar(KB_PDS_FULL), g_it & 1, abort)) { failed = true; break; }
+          if (first && !mbar_wait_relaxed(bar(KB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tmem + K_T_DV, tmem + K_T_S + kk * 8, sdesc_sw128(da + kk * 2048, kHalf, 1024), id_mn,
+                        (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tmem + K_T_DK, tmem + K_T_DP + kk * 8, sdesc_sw128(qa + kk * 2048, kHalf, 1024), id_mn,
+                        (!first || kk > 0) ? 1u : 0u);
+          mma_commit(bar(KB_QD_EMPTY + st));
+          first = false;
+        }
+        if (failed) break;
+        mma_commit(bar(KB_KV_EMPTY));
+        mma_commit(bar(KB_ACC_DONE));
+        ++unit_it;
+      }
+      if (failed) raise_abort(abort, 0x200);
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise (warps 0-3)
+    const int r = threadIdx.x;  // key of the tile == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t qd_it = 0, g_it = 0, unit_it = 0;
+    bool failed = false;
+    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+      const BwdItem it = p.plan.items[u / p.Hkv];
+      const int g = u % p.Hkv;
+      QIter q;
+      if (!q_begin(p, it, q)) continue;
+      const int32_t key = it.k_start + r;
+      for (bool ok = true; ok; ok = q_next(p, q), ++qd_it, ++g_it) {
+        // the row data was written by the producer before it armed QD_FULL
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_QD_FULL + (qd_it & 1)), (qd_it >> 1) & 1, abort))) {
+          failed = true;
+          break;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_SP_FULL), g_it & 1, abort))) { failed = true; break; }
+        tc_fence_after();
+        const float* rd = rowdata + (qd_it & 1) * 256;
+        // row c (token t0 + c % tt) sees this key iff the token index i = c % tt
+        // lies in [i_lo, i_hi)
+        const bool key_ok = key >= q.be.k_lo && key < q.be.k_hi;
+        const int i_lo = q.be.causal ? max(0, key - q.t0) : 0;
+        const int i_hi = key_ok ? min(tt, q.be.q_hi - q.t0) : 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32], dv[32], pp[16], dd[16];
+          tmem_ld32(tmem + lb + K_T_S + c * 32, sv);
+          tmem_ld32(tmem + lb + K_T_DP + c * 32, dv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int col = c * 32 + i;
+            const int i0 = col & (tt - 1), i1 = (col + 1) & (tt - 1);
+            const float p0 = (i0 >= i_lo && i0 < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i]), p.sl2, -rd[col])) : 0.f;
+            const float p1 =
+                (i1 >= i_lo && i1 < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.sl2, -rd[col + 1])) : 0.f;
+            pp[i >> 1] = pack_bf16x2(p0, p1);
+            dd[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[i]) - rd[128 + col]),
+                                     p1 * (__uint_as_float(dv[i + 1]) - rd[128 + col + 1]));
+          }
+          // P^T and dS^T as bf16 pairs over columns already read
+          tmem_st16(tmem + lb + K_T_S + c * 16, pp);
+          tmem_st16(tmem + lb + K_T_DP + c * 16, dd);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KB_PDS_FULL));
+      }
+      if (failed) break;
+      // epilogue: dV and dK of this key
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_ACC_DONE), unit_it & 1, abort))) { failed = true; break; }
+      tc_fence_after();
+      const bool valid = r < it.k_len;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        __nv_bfloat16* out = part == 0 ? p.dv : p.dk;
+        const float mul = part == 0 ? 1.f : p.scale;
+        const uint32_t col0 = part == 0 ? K_T_DV : K_T_DK;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lb + col0 + c * 32, v);
+          tmem_wait_ld();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(key) * p.Hkv + g) * kHeadDim + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * mul, __uint_as_float(v[8 * i + 1]) * mul),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 2]) * mul, __uint_as_float(v[8 * i + 3]) * mul),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 4]) * mul, __uint_as_float(v[8 * i + 5]) * mul),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 6]) * mul, __uint_as_float(v[8 * i + 7]) * mul));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(KB_ACC_FREE));
+      ++unit_it;
+    }
+    if (failed && lane == 0) raise_abort(abort, 0x400);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+int make_map(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, cuuint64_t heads, cuuint64_t T, cuuint32_t rows,
+             std::string* err) {
+  const cuuint64_t dims[3] = {128, heads, T};
+  const cuuint64_t strides[2] = {256, heads * 256};
+  const cuuint32_t box[3] = {64, 1, rows};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed with code " + std::to_string(static_cast<int>(r));
+    return PADOC_ERR_CUDA;
+  }
+  return PADOC_OK;
+}
+
+}  // namespace
+
+int launch_bwd_tc(const BwdArgs& a, cudaStream_t s, std::string* err) {
+  int rc = launch_bwd_delta(a, PADOC_BF16, s, err);
+  if (rc) return rc;
+  EncodeTiledFn enc = get_encode_fn(err);
+  if (!enc) return PADOC_ERR_CUDA;
+  const int tt = a.fwd.tile_tokens;
+  CUtensorMap mq, mdo, mk, mv;
+  rc = make_map(enc, &mq, a.q, a.Hq, a.T, tt, err);
+  if (!rc) rc = make_map(enc, &mdo, a.dout, a.Hq, a.T, tt, err);
+  if (!rc) rc = make_map(enc, &mk, a.k, a.Hkv, a.T, 128, err);
+  if (!rc) rc = make_map(enc, &mv, a.v, a.Hkv, a.T, 128, err);
+  if (rc) return rc;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDkvSmem);
+    if (e != cudaSuccess) {
+      *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+      return PADOC_ERR_CUDA;
+    }
+    attr = true;
+  }
+  const float sl2 = a.scale * kLog2e;
+  if (a.fwd.n_items > 0) {
+    DqParams p{};
+    p.plan = a.fwd;
+    p.n_units = a.fwd.n_items * a.Hkv;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.group = a.fwd.group;
+    p.T = a.T;
+    p.sl2 = sl2;
+    p.scale = a.scale;
+    p.lse = a.lse;
+    p.delta = a.delta;
+    p.dq = static_cast<__nv_bfloat16*>(a.dq);
+    bwd_dq_kernel<<<std::min(p.n_units, num_sms()), kThreads, kDqSmem, s>>>(mq, mdo, mk, mv, p);
+  }
+  if (a.bwd.n_items > 0) {
+    DkvParams p{};
+    p.plan = a.bwd;
+    p.n_units = a.bwd.n_items * a.Hkv;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.group = a.fwd.group;
+    p.tile_tokens = tt;
+    p.T = a.T;
+    p.sl2 = sl2;
+    p.scale = a.scale;
+    p.lse = a.lse;
+    p.delta = a.delta;
+    p.dk = static_cast<__nv_bfloat16*>(a.dk);
+    p.dv = static_cast<__nv_bfloat16*>(a.dv);
+    bwd_dkv_kernel<<<std::min(p.n_units, num_sms()), kThreads, kDkvSmem, s>>>(mq, mdo, mk, mv, p);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string("backward kernel launch: ") + cudaGetErrorString(e);
+    return PADOC_ERR_CUDA;
+  }
+  return PADOC_OK;
+}
+
+int read_and_clear_bwd_error(cudaStream_t s, unsigned* word) {
+  unsigned zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_bwd_err, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_bwd_err, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? PADOC_OK : PADOC_ERR_CUDA;
+}
+
+}  // namespace padoc

@@ -171,6 +171,19 @@ __global__ void __launch_bounds__(kWarps * 32) dkv_core_kernel(BwdPlan plan, int
 }
 
 template <typename T, int D>
+int launch_delta(const BwdArgs& a, cudaStream_t s, std::string* err) {
+  const int64_t warps = a.T * a.Hq;
+  delta_kernel<T, D><<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, s>>>(
+      static_cast<const T*>(a.o), static_cast<const T*>(a.dout), a.delta, a.T, a.Hq);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string("delta launch: ") + cudaGetErrorString(e);
+    return PADOC_ERR_CUDA;
+  }
+  return PADOC_OK;
+}
+
+template <typename T, int D>
 int launch_typed(const BwdArgs& a, cudaStream_t s, std::string* err) {
   const T* q = static_cast<const T*>(a.q);
   const T* k = static_cast<const T*>(a.k);
@@ -195,6 +208,12 @@ int launch_typed(const BwdArgs& a, cudaStream_t s, std::string* err) {
 }
 
 }  // namespace
+
+int launch_bwd_delta(const BwdArgs& a, int32_t dtype, cudaStream_t s, std::string* err) {
+  if (dtype == PADOC_BF16)
+    return a.d == 128 ? launch_delta<__nv_bfloat16, 128>(a, s, err) : launch_delta<__nv_bfloat16, 64>(a, s, err);
+  return a.d == 128 ? launch_delta<float, 128>(a, s, err) : launch_delta<float, 64>(a, s, err);
+}
 
 int launch_bwd_core(const BwdArgs& a, int32_t dtype, cudaStream_t s, std::string* err) {
   if (dtype == PADOC_BF16)

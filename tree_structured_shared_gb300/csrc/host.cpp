@@ -510,7 +510,13 @@ extern "C" int padoc_tree_attn_varlen_bwd(padoc_tree_desc* desc, const void* q, 
   a.d = d;
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
   std::string err;
-  rc = launch_bwd_core(a, dtype, reinterpret_cast<cudaStream_t>(stream), &err);
+  // bf16 at d = 128 runs on the tensor cores; PADOC_BWD_CORE=1 selects the
+  // CUDA-core kernels instead (a second implementation to compare against)
+  static const bool force_core = std::getenv("PADOC_BWD_CORE") && std::atoi(std::getenv("PADOC_BWD_CORE")) != 0;
+  if (dtype == PADOC_BF16 && d == kHeadDim && !force_core)
+    rc = launch_bwd_tc(a, reinterpret_cast<cudaStream_t>(stream), &err);
+  else
+    rc = launch_bwd_core(a, dtype, reinterpret_cast<cudaStream_t>(stream), &err);
   if (rc) return fail(rc, "tree_attn_varlen_bwd: %s", err.c_str());
   return PADOC_OK;
 }
@@ -1275,9 +1281,11 @@ extern "C" int padoc_depths(const int32_t* layout_len, const int32_t* content_le
 }
 
 extern "C" int padoc_device_status(padoc_stream_t stream) {
-  unsigned w = 0;
-  const int rc = read_and_clear_tc_error(reinterpret_cast<cudaStream_t>(stream), &w);
+  unsigned w = 0, wb = 0;
+  int rc = read_and_clear_tc_error(reinterpret_cast<cudaStream_t>(stream), &w);
+  if (!rc) rc = read_and_clear_bwd_error(reinterpret_cast<cudaStream_t>(stream), &wb);
   if (rc) return fail(rc, "device_status: could not read the device error word");
+  w |= wb;
   if (w) return fail(PADOC_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (site mask 0x%x)", w);
   return PADOC_OK;
 }

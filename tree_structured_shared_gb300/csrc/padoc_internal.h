@@ -151,6 +151,9 @@ int launch_commit(void* k_pool, void* v_pool, const void* plan, int64_t n_rows, 
                   const void* v, cudaStream_t s, std::string* err);
 
 int launch_bwd_core(const BwdArgs& a, int32_t dtype, cudaStream_t s, std::string* err);
+int launch_bwd_delta(const BwdArgs& a, int32_t dtype, cudaStream_t s, std::string* err);
+int launch_bwd_tc(const BwdArgs& a, cudaStream_t s, std::string* err);
+int read_and_clear_bwd_error(cudaStream_t s, unsigned* word);
 
 // Device error words (set by kernels that give up a bounded wait).
 int read_and_clear_tc_error(cudaStream_t s, unsigned* word);
