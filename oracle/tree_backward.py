@@ -28,7 +28,7 @@ import math
 
 import numpy as np
 
-from .tree_attention import PACK_CANONICAL, ancestor_positions
+from .tree_attention import PACK_CANONICAL, _ancestor_identities, ancestor_positions, packed_layout
 
 
 def _attend_grad(q, K, V, dO, scale):
@@ -56,11 +56,14 @@ def _attend_grad(q, K, V, dO, scale):
     return dq, dK, dV
 
 
-def tree_backward(q, k, v, dO, pages, order: int = PACK_CANONICAL, scale=None):
+def tree_backward(q, k, v, dO, pages, order: int = PACK_CANONICAL, scale=None, positions=None):
     """Gradients of sum(dO * O) for the tree-varlen forward.
 
     q, dO [T, Hq, d]; k, v [T, Hkv, d] (any float dtype; float64 inside).
-    Returns dQ [T, Hq, d], dK [T, Hkv, d], dV [T, Hkv, d] in float64."""
+    Returns dQ [T, Hq, d], dK [T, Hkv, d], dV [T, Hkv, d] in float64.
+    `positions` limits the work to those query positions: their dQ rows are
+    exact (the rest stay NaN) and dK / dV hold only their contributions,
+    which is the whole gradient for any key that no other query sees."""
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
@@ -68,12 +71,24 @@ def tree_backward(q, k, v, dO, pages, order: int = PACK_CANONICAL, scale=None):
     T, Hq, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    anc = ancestor_positions(pages, order)
-    assert len(anc) == T
-    dQ = np.zeros_like(q)
+    if positions is None:
+        anc = ancestor_positions(pages, order)
+        assert len(anc) == T
+        rows = range(T)
+        dQ = np.zeros_like(q)
+    else:
+        ident, pos = packed_layout(pages, order)
+        assert len(ident) == T
+        rows = list(positions)
+        anc = {}
+        for t in rows:
+            p, kind, r, i = ident[t]
+            a = _ancestor_identities(pages[p], p, kind, r, i)
+            anc[t] = np.sort(np.fromiter((pos[x] for x in a), dtype=np.int64, count=len(a)))
+        dQ = np.full_like(q, np.nan)
     dK = np.zeros_like(k)
     dV = np.zeros_like(v)
-    for t in range(T):
+    for t in rows:
         a = anc[t]
         dq, dk, dv = _attend_grad(q[t], k[a], v[a], dO[t], scale)
         dQ[t] = dq

@@ -65,3 +65,65 @@ def test_deterministic(padoc_lib):
     torch.cuda.synchronize()
     for a, c in zip(first, (b.dq, b.dk, b.dv)):
         assert torch.equal(a, c)
+
+
+def test_cuda_core_path_bf16(padoc_lib, tmp_path):
+    """The CUDA-core kernels (selected by PADOC_BWD_CORE=1) on a bf16 case
+    the tensor-core path also serves; run in a child process because the
+    switch is read once per process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = tmp_path / "grads.npz"
+    code = (
+        "import sys, numpy as np, torch; sys.path.insert(0, %r)\n"
+        "from tree_structured_shared_gb300 import harness, workloads as wl\n"
+        "w = wl.random_pages(81, n_pages=2, max_prefix=200, max_regions=4, max_layout=12, max_content=120,"
+        " allow_empty=False, Hq=4, Hkv=2, d=128, dtype='bf16')\n"
+        "q, k, v = wl.tree_qkv(w, 2)\n"
+        "d_o = wl.round_bf16(wl.normal_f32(13, (w.n_tokens, 4, 128), w.value_scale))\n"
+        "f = harness.Forward(w, q, k, v); f.run(); b = harness.Backward(f, d_o); b.run(); torch.cuda.synchronize()\n"
+        "np.savez(%r, *[x.float().cpu().numpy() for x in (b.dq, b.dk, b.dv)])\n"
+    ) % (root, str(out))
+    env = dict(os.environ, PADOC_BWD_CORE="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    got = np.load(out)
+    w = wl.random_pages(81, n_pages=2, max_prefix=200, max_regions=4, max_layout=12, max_content=120,
+                        allow_empty=False, Hq=4, Hkv=2, d=128, dtype="bf16")
+    q, k, v = wl.tree_qkv(w, 2)
+    d_o = wl.round_bf16(wl.normal_f32(13, (w.n_tokens, 4, 128), w.value_scale))
+    ref = tb.tree_backward(q, k, v, d_o, w.pages)
+    for i, name in enumerate(("dq", "dk", "dv")):
+        check_grad(got[f"arr_{i}"], ref[i], "bf16", f"core {name}")
+
+
+def test_packed_backward_sampled_regions(padoc_lib):
+    """The bench's training workload, 8 packed sequences of 16384 tokens, in
+    one backward launch; checked on the tokens of sampled content regions.
+    A content token's key is seen only by later tokens of its own region, so
+    the oracle restricted to those queries gives their dQ, dK and dV."""
+    import torch
+    from oracle import tree_attention as ta
+    from tree_structured_shared_gb300 import harness
+    fw = wl.packed_sequences(0)
+    f = harness.Forward(fw, seed=0)
+    f.run()
+    b = harness.Backward(f, seed=0)
+    b.run()
+    torch.cuda.synchronize()
+    padoc.device_status()
+    starts = np.cumsum([0] + [p.n_tokens for p in fw.pages])
+    for pi in [1, len(fw.pages) // 2, len(fw.pages) - 2]:
+        a, e = int(starts[pi]), int(starts[pi + 1])
+        page = [fw.pages[pi]]
+        ident, _ = ta.packed_layout(page)
+        N = len(page[0].layout_len)
+        regions = [r for r in range(N) if page[0].content_len[r] > 0]
+        for r in (regions[0], regions[-1]):
+            rows = [t for t, (_, kind, rr, _) in enumerate(ident) if kind == ta.Y_KIND and rr == r]
+            host = [x[a:e].float().cpu().numpy() for x in (f.q, f.k, f.v, b.d_o)]
+            ref = tb.tree_backward(*host, page, positions=rows)
+            for g, rr_, name in zip((b.dq, b.dk, b.dv), ref, ("dq", "dk", "dv")):
+                check_grad(g[a:e].float().cpu().numpy()[rows], rr_[rows], "bf16", f"page {pi} region {r} {name}")

@@ -105,3 +105,19 @@ def test_isolation():
     assert np.all(dQ[~in_yj] == 0)
     assert np.all(dK[~anc] == 0) and np.all(dV[~anc] == 0)
     assert np.abs(dV[anc]).sum() > 0
+
+
+def test_restricted_positions_match_full():
+    """Restricting the query positions reproduces the full result on those
+    rows, and on keys that only those queries see."""
+    w, q, k, v, dO = _case(8, n_pages=2, max_prefix=6, max_regions=3, max_layout=3, max_content=6)
+    full = tb.tree_backward(q, k, v, dO, w.pages)
+    ident, _ = ta.packed_layout(w.pages)
+    # the last content region of page 0: its keys are seen by its own tokens only
+    p0 = w.pages[0]
+    N = len(p0.layout_len)
+    rows = [t for t, (p, kind, r, _) in enumerate(ident) if p == 0 and kind == ta.Y_KIND and r == N - 1]
+    part = tb.tree_backward(q, k, v, dO, w.pages, positions=rows)
+    np.testing.assert_allclose(part[0][rows], full[0][rows], atol=1e-13, rtol=0)
+    np.testing.assert_allclose(part[1][rows], full[1][rows], atol=1e-13, rtol=0)
+    np.testing.assert_allclose(part[2][rows], full[2][rows], atol=1e-13, rtol=0)
