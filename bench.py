@@ -7,11 +7,12 @@ A step runs both regimes of the hot path on the serving-scale workload:
     page (zero-copy forks of the page prefix), own suffix U[0, 1024], one
     query token per live branch (about 17.6 k branches); kernels: the cascade
     prefix pass and the own-suffix pass with the log-sum-exp merge;
-  * tree-varlen forward: 8 packed sequences of 16384 tokens built from the
-    same page-length distributions.
+  * tree-varlen forward and its backward (dQ, dK, dV): 8 packed sequences of
+    16384 tokens built from the same page-length distributions.
 `value` is branch-decode attention tokens per second (query tokens of all
-ranks divided by the slowest rank's decode time); the forward's TFLOP/s and
-both roofline fractions ride along in the same JSON line.
+ranks divided by the slowest rank's decode time); the forward's and the
+backward's TFLOP/s and the roofline fractions ride along in the same JSON
+line.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -42,8 +43,8 @@ WORKLOADS = {
 
 
 def workload_name(kind: str, fwd_seqs: int) -> str:
-    return (WORKLOADS[kind] + f" + tree-varlen forward over {fwd_seqs} x 16384 packed tokens; bf16, Hq=16, "
-            "Hkv=8, d=128")
+    return (WORKLOADS[kind] + f" + tree-varlen forward and backward over {fwd_seqs} x 16384 packed tokens; "
+            "bf16, Hq=16, Hkv=8, d=128")
 
 
 WORKLOAD = workload_name("serving", 8)
@@ -268,6 +269,7 @@ def main() -> int:
     fw = wl.packed_sequences(seed, n_seq=args.fwd_seqs)
     dec = harness.Decode(dw, seed=seed, tree=args.workload == "verify")
     fwd = harness.Forward(fw, seed=seed)
+    bwd = harness.Backward(fwd, seed=seed)
     dec.plan()
     stream = torch.cuda.current_stream()
     acc = None
@@ -285,11 +287,12 @@ def main() -> int:
         dec.own_pass()
         accept_step()
         fwd.run()
+        bwd.run()
     torch.cuda.synchronize()
     padoc.device_status()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.2)
@@ -306,6 +309,8 @@ def main() -> int:
         ev[s][3].record(stream)
         fwd.run()
         ev[s][4].record(stream)
+        bwd.run()
+        ev[s][5].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -315,11 +320,12 @@ def main() -> int:
     t_own = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     t_acc = sum(e[2].elapsed_time(e[3]) for e in ev) / K
     t_fwd = sum(e[3].elapsed_time(e[4]) for e in ev) / K
+    t_bwd = sum(e[4].elapsed_time(e[5]) for e in ev) / K
     t_dec = t_pre + t_own
-    times = torch.tensor([t_dec, t_fwd, t_pre, t_own, t_acc], dtype=torch.float64, device="cuda")
+    times = torch.tensor([t_dec, t_fwd, t_pre, t_own, t_acc, t_bwd], dtype=torch.float64, device="cuda")
     if world > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_dec, t_fwd, t_pre, t_own, t_acc = [float(x) for x in times.tolist()]
+    t_dec, t_fwd, t_pre, t_own, t_acc, t_bwd = [float(x) for x in times.tolist()]
 
     # end to end through the all-in-one C-ABI call, inputs from pinned host memory
     e2e = None
@@ -393,7 +399,8 @@ def main() -> int:
                    "forward_tokens": fw.n_tokens,
                    "l2": "inputs larger than L2 (decode KV about 48 GB, forward Q/K/V 1.3 GB)",
                    "step": ("value and ms_per_step cover the decode step (prefix pass + own pass); the forward "
-                            "runs in the same timed loop and is reported under 'forward'"),
+                            "and its backward run in the same timed loop and are reported under 'forward' and "
+                            "'backward'"),
                    "parallelism": f"dp{world} (independent pages per GPU)"},
         "roofline": {"bound": "hbm", "kernel": "own_pass_kernel", "achieved": own_gbs, "peak": hbm,
                      "unit": "GB/s", "frac": own_gbs / hbm, "peak_source": peak_src,
@@ -411,7 +418,12 @@ def main() -> int:
                     "peak": tf_sus, "peak_kind": "bf16 sustained " + peak_src, "frac": fwd_tf / tf_sus,
                     "frac_spec_2250": fwd_tf / 2250.0, "algorithmic_flops": fl,
                     "traffic": traffic_for("forward", fw.n_tokens)},
-        "gpu_launches": (5 if acc is not None else 3) * K,
+        "backward": {"ms": t_bwd, "tflops": bwd.flops / (t_bwd * 1e-3) / 1e12 * world,
+                     "tflops_per_gpu": bwd.flops / (t_bwd * 1e-3) / 1e12, "bound": "tensor", "peak": tf_sus,
+                     "peak_kind": "bf16 sustained " + peak_src,
+                     "frac": bwd.flops / (t_bwd * 1e-3) / 1e12 / tf_sus, "algorithmic_flops": bwd.flops,
+                     "what": "dQ, dK, dV of the same forward (launches: row sums, dQ pass, dK/dV pass)"},
+        "gpu_launches": ((5 if acc is not None else 3) + 3) * K,
         "clocks": clk,
     }
     if acc is not None:
