@@ -18,8 +18,11 @@
 //                     dV += P^T dO, dK += dS^T Q         (tensor cores, A in TMEM)
 // Neither kernel needs atomics: every output row belongs to one unit.
 //
-// Roles (192 threads): warps 0-3 element-wise work and epilogue, warp 4 TMA
-// producer, warp 5 MMA issuer (one thread).  Every wait is bounded; a timed
+// Roles (320 threads): warps 0-7 element-wise work and epilogue (two
+// warpgroups; warp w reads TMEM lanes 32 (w % 4) .. + 31, warpgroup w / 4
+// takes one half of the tile's columns), warp 8 TMA producer, warp 9 MMA
+// issuer (one thread).  The MMA thread starts the products of a column half
+// as soon as that half's warpgroup is done with it.  Every wait is bounded; a timed
 // out wait raises the CTA abort flag and this file's device error word.
 #include <cuda_bf16.h>
 
@@ -38,7 +41,9 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kHalf = 16384;  // one 64-column half of a 128-row bf16 tile
 constexpr int kTile = 2 * kHalf;
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -86,12 +91,14 @@ enum {
   QB_QD_EMPTY = 1,
   QB_KV_FULL = 2,   // +stage (2)
   QB_KV_EMPTY = 4,  // +stage (2)
-  QB_SP_FULL = 6,
-  QB_SPARE = 7,
-  QB_DS_FULL = 8,   // count 4
-  QB_DQ_DONE = 9,
-  QB_ACC_FREE = 10,  // count 4
-  QB_N = 11
+  QB_SP_FULL = 6,   // S and dP of the tile are in TMEM
+  QB_RD = 7,        // count 8: both warpgroups have read them (the columns are free)
+  // per key half h (columns 64h .. 64h + 63 of S and dP, warpgroup h):
+  QB_DS_FULL = 8,   // +h, count 4: dS of the half is in TMEM
+  QB_DQ_DONE = 10,  // +h: dQ += dS K over the half has run (the dS columns are free)
+  QB_DQ_ALL = 12,   // the unit's dQ is complete
+  QB_ACC_FREE = 13,  // count 8: the epilogue has read dQ
+  QB_N = 14
 };
 
 struct DqUnit {
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_N; ++i)
-      mbar_init(bar(i), (i == QB_DS_FULL || i == QB_ACC_FREE) ? 4u : 1u);
+      mbar_init(bar(i), (i == QB_DS_FULL || i == QB_DS_FULL + 1) ? 4u : ((i == QB_ACC_FREE || i == QB_RD) ? 8u : 1u));
     *abort = 0;
     fence_mbar_init();
   }
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int G = p.group, tt = p.plan.tile_tokens;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -211,25 +218,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (failed) raise_abort(abort, 0x10);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);  // both K-major
       constexpr uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);   // B MN-major
       uint32_t kv_it = 0, g_it = 0, unit_it = 0;
       bool failed = false;
-      auto issue_dq = [&](uint32_t tile_it, bool first) -> bool {
-        // dQ += dS K for tile tile_it (dS in TMEM, K of its stage as MN-major B)
-        if (!mbar_wait_relaxed(bar(QB_DS_FULL), tile_it & 1, abort)) return false;
-        tc_fence_after();
+      auto issue_dq = [&](uint32_t tile_it, bool first, bool last) -> bool {
+        // dQ += dS K for tile tile_it (dS in TMEM, K of its stage as MN-major
+        // B), one key half at a time as each warpgroup finishes its dS
+        if (first && !mbar_wait_relaxed(bar(QB_ACC_FREE), (unit_it & 1) ^ 1, abort)) return false;
         const int st = tile_it & 1;
         const uint32_t ka = sbase + Q_SM_K + st * kTile;
+        for (int half = 0; half < 2; ++half) {
+          if (!mbar_wait_relaxed(bar(QB_DS_FULL + half), tile_it & 1, abort)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + Q_T_DQ, tmem + Q_T_DS + kk * 8, sdesc_sw128(ka + kk * 2048, kHalf, 1024), id_mn,
-                      (!first || kk > 0) ? 1u : 0u);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = half * 4 + k4;
+            mma_bf16_ts(tmem + Q_T_DQ, tmem + Q_T_DS + kk * 8, sdesc_sw128(ka + kk * 2048, kHalf, 1024), id_mn,
+                        (!first || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(QB_DQ_DONE + half));
+        }
         mma_commit(bar(QB_KV_EMPTY + st));
-        mma_commit(bar(QB_DQ_DONE));
+        if (last) mma_commit(bar(QB_DQ_ALL));
         return true;
       };
       for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
@@ -239,16 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_relaxed(bar(QB_QD_FULL), unit_it & 1, abort)) { failed = true; break; }
         const uint32_t qa = sbase + Q_SM_Q, da = sbase + Q_SM_DO;
         for (int j = 0; j < n; ++j, ++kv_it, ++g_it) {
-          // dQ of the previous tile first: once its dS is in, the S and dP
-          // columns are free too (the element-wise warps read them before)
-          if (j > 0) {
-            if (j == 1 && !mbar_wait_relaxed(bar(QB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
-            if (!issue_dq(g_it - 1, j == 1)) { failed = true; break; }
-          }
           const int st = kv_it & 1;
           if (!mbar_wait_relaxed(bar(QB_KV_FULL + st), (kv_it >> 1) & 1, abort)) { failed = true; break; }
-          tc_fence_after();
           const uint32_t ka = sbase + Q_SM_K + st * kTile, va = sbase + Q_SM_V + st * kTile;
+          // S and dP go over columns both warpgroups have read (they compute the
+          // previous tile's dS from registers meanwhile)
+          if (g_it > 0 && !mbar_wait_relaxed(bar(QB_RD), (g_it - 1) & 1, abort)) { failed = true; break; }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -263,19 +274,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(bar(QB_SP_FULL));
           if (j == n - 1) mma_commit(bar(QB_QD_EMPTY));
+          if (j > 0 && !issue_dq(g_it - 1, j == 1, false)) { failed = true; break; }
         }
         if (failed) break;
-        if (n == 1 && !mbar_wait_relaxed(bar(QB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
-        if (!issue_dq(g_it - 1, n == 1)) { failed = true; break; }
+        if (!issue_dq(g_it - 1, n == 1, true)) { failed = true; break; }
         ++unit_it;
       }
       if (failed) raise_abort(abort, 0x20);
     }
   } else {
-    // ------------------------------------------------------------ element-wise (warps 0-3)
-    const int r = threadIdx.x;  // query row == TMEM lane
-    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t g_it = 0;
+    // ------------------------------------------------------------ element-wise (warps 0-7)
+    const int wg = warp >> 2;                    // column half of this warpgroup
+    const int r = (warp & 3) * 32 + lane;        // query row == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t g_it = 0, unit_it = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
       const DqUnit w = dq_unit(p, u);
@@ -294,43 +306,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t klen = min(kTileKeys, t.end - t.ks);
         int32_t vis = valid ? klen : 0;
         if (t.causal) vis = min(vis, static_cast<int32_t>(qpos + 1 - t.ks));
-        // dS goes over the previous tile's dS: that tile's dQ completed before
-        // this tile's S (tensor operations complete in issue order)
-        if (g_it > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_DQ_DONE), (g_it - 1) & 1, abort))) { failed = true; break; }
-          tc_fence_after();
-        }
+        vis -= wg * 64;  // in this half's column numbering
+        uint32_t sv[2][32], dv[2][32];
+        tmem_ld32(tmem + lb + Q_T_S + wg * 64, sv[0]);
+        tmem_ld32(tmem + lb + Q_T_DP + wg * 64, dv[0]);
+        tmem_ld32(tmem + lb + Q_T_S + wg * 64 + 32, sv[1]);
+        tmem_ld32(tmem + lb + Q_T_DP + wg * 64 + 32, dv[1]);
+        tmem_wait_ld();
+        // the half's S and dP columns may take the next tile's products now
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_RD));
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32], dv[32], pk[16];
-          tmem_ld32(tmem + lb + Q_T_S + c * 32, sv);
-          tmem_ld32(tmem + lb + Q_T_DP + c * 32, dv);
-          tmem_wait_ld();
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             const int col = c * 32 + i;
-            const float p0 = col < vis ? fast_exp2(fmaf(__uint_as_float(sv[i]), p.sl2, -lse2)) : 0.f;
-            const float p1 = col + 1 < vis ? fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.sl2, -lse2)) : 0.f;
-            pk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[i]) - Dr), p1 * (__uint_as_float(dv[i + 1]) - Dr));
+            const float p0 = col < vis ? fast_exp2(fmaf(__uint_as_float(sv[c][i]), p.sl2, -lse2)) : 0.f;
+            const float p1 = col + 1 < vis ? fast_exp2(fmaf(__uint_as_float(sv[c][i + 1]), p.sl2, -lse2)) : 0.f;
+            pk[col >> 1] =
+                pack_bf16x2(p0 * (__uint_as_float(dv[c][i]) - Dr), p1 * (__uint_as_float(dv[c][i + 1]) - Dr));
           }
-          tmem_st16(tmem + lb + Q_T_DS + c * 16, pk);
         }
+        // dS goes over the previous tile's dS once that tile's dQ has read it
+        if (g_it > 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_DQ_DONE + wg), (g_it - 1) & 1, abort))) { failed = true; break; }
+          tc_fence_after();
+        }
+        tmem_st32(tmem + lb + Q_T_DS + wg * 32, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(QB_DS_FULL));
+        if (lane == 0) mbar_arrive(bar(QB_DS_FULL + wg));
       }
       if (failed) break;
-      // epilogue: dQ of this row
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_DQ_DONE), (g_it - 1) & 1, abort))) { failed = true; break; }
+      // epilogue: this warpgroup's half of the row's dQ
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_DQ_ALL), unit_it & 1, abort))) { failed = true; break; }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lb + Q_T_DQ + c * 32, v);
+        tmem_ld32(tmem + lb + Q_T_DQ + wg * 64 + c * 32, v);
         tmem_wait_ld();
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dq + (qpos * p.Hq + head) * kHeadDim + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(p.dq + (qpos * p.Hq + head) * kHeadDim + wg * 64 + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * p.scale, __uint_as_float(v[8 * i + 1]) * p.scale),
@@ -342,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(QB_ACC_FREE));
+      ++unit_it;
     }
     if (failed && lane == 0) raise_abort(abort, 0x40);
   }
@@ -365,11 +386,12 @@ enum {
   KB_KV_EMPTY = 1,
   KB_QD_FULL = 2,   // +stage (2)
   KB_QD_EMPTY = 4,  // +stage (2)
-  KB_SP_FULL = 6,
-  KB_PDS_FULL = 7,  // count 4
-  KB_ACC_DONE = 8,
-  KB_ACC_FREE = 9,  // count 4
-  KB_N = 10
+  KB_SP_FULL = 6,   // S^T and dP^T of the tile are in TMEM
+  // per query-row half h (columns 64h .. 64h + 63 of S^T and dP^T, warpgroup h):
+  KB_PDS_FULL = 7,  // +h, count 4: P^T and dS^T of the half are in TMEM
+  KB_ACC_DONE = 9,
+  KB_ACC_FREE = 10,  // count 8
+  KB_N = 11
 };
 
 // Query tiles of a key tile: each entry's queries in steps of tile_tokens.
@@ -408,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   if (threadIdx.x == 0) {
-    for (int i = 0; i < KB_N; ++i) mbar_init(bar(i), (i == KB_PDS_FULL || i == KB_ACC_FREE) ? 4u : 1u);
+    for (int i = 0; i < KB_N; ++i)
+      mbar_init(bar(i), (i == KB_PDS_FULL || i == KB_PDS_FULL + 1) ? 4u : (i == KB_ACC_FREE ? 8u : 1u));
     *abort = 0;
     fence_mbar_init();
   }
@@ -422,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int G = p.group, tt = p.tile_tokens;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -476,53 +499,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++unit_it;
     }
     if (failed && lane == 0) raise_abort(abort, 0x100);
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);
-      uint32_t qd_it = 0, g_it = 0, unit_it = 0;
+      uint32_t qd_it = 0, unit_it = 0;
       bool failed = false;
+      const uint32_t ka = sbase + K_SM_K, va = sbase + K_SM_V;
+      // S^T = K Q^T and dP^T = V dO^T for the tile in stage st
+      auto issue_s = [&](int st) {
+        const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile, da = qa + kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          mma_bf16_ss(tmem + K_T_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), id_kk,
+                      kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          mma_bf16_ss(tmem + K_T_DP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), id_kk,
+                      kk > 0);
+        }
+        mma_commit(bar(KB_SP_FULL));
+      };
       for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
         const BwdItem it = p.plan.items[u / p.Hkv];
         QIter q;
         if (!q_begin(p, it, q)) continue;
         if (!mbar_wait_relaxed(bar(KB_KV_FULL), unit_it & 1, abort)) { failed = true; break; }
-        const uint32_t ka = sbase + K_SM_K, va = sbase + K_SM_V;
+        if (!mbar_wait_relaxed(bar(KB_QD_FULL + (qd_it & 1)), (qd_it >> 1) & 1, abort)) { failed = true; break; }
+        tc_fence_after();
+        issue_s(qd_it & 1);
         bool first = true;
-        for (bool ok = true; ok; ok = q_next(p, q), ++qd_it, ++g_it) {
+        for (bool ok = true; ok; ++qd_it) {
           const int st = qd_it & 1;
-          if (!mbar_wait_relaxed(bar(KB_QD_FULL + st), (qd_it >> 1) & 1, abort)) { failed = true; break; }
-          tc_fence_after();
           const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile, da = qa + kTile;
-          // S^T = K Q^T and dP^T = V dO^T; the previous tile's dV / dK MMAs,
-          // which read P^T / dS^T from these columns, were issued earlier
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            mma_bf16_ss(tmem + K_T_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), id_kk,
-                        kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            mma_bf16_ss(tmem + K_T_DP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), id_kk,
-                        kk > 0);
-          }
-          mma_commit(bar(KB_SP_FULL));
-          if (!mbar_wait_relaxed(bar(KB_PDS_FULL), g_it & 1, abort)) { failed = true; break; }
+          const bool more = q_next(p, q);
           if (first && !mbar_wait_relaxed(bar(KB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
-          tc_fence_after();
+          for (int half = 0; half < 2; ++half) {
+            // dV += P^T dO and dK += dS^T Q over the half's query rows (warpgroup
+            // h packed rows 64h .. 64h + 63 into columns 64h .. 64h + 31)
+            if (!mbar_wait_relaxed(bar(KB_PDS_FULL + half), qd_it & 1, abort)) { failed = true; break; }
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + K_T_DV, tmem + K_T_S + kk * 8, sdesc_sw128(da + kk * 2048, kHalf, 1024), id_mn,
-                        (!first || kk > 0) ? 1u : 0u);
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int kk = half * 4 + k4;
+              mma_bf16_ts(tmem + K_T_DV, tmem + K_T_S + half * 64 + k4 * 8, sdesc_sw128(da + kk * 2048, kHalf, 1024),
+                          id_mn, (!first || kk > 0) ? 1u : 0u);
+            }
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + K_T_DK, tmem + K_T_DP + kk * 8, sdesc_sw128(qa + kk * 2048, kHalf, 1024), id_mn,
-                        (!first || kk > 0) ? 1u : 0u);
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int kk = half * 4 + k4;
+              mma_bf16_ts(tmem + K_T_DK, tmem + K_T_DP + half * 64 + k4 * 8, sdesc_sw128(qa + kk * 2048, kHalf, 1024),
+                          id_mn, (!first || kk > 0) ? 1u : 0u);
+            }
+          }
+          if (failed) break;
           mma_commit(bar(KB_QD_EMPTY + st));
+          // the next tile's S^T / dP^T over the columns just consumed (the
+          // products above read them first: tensor operations run in order)
+          if (more) {
+            if (!mbar_wait_relaxed(bar(KB_QD_FULL + ((qd_it + 1) & 1)), ((qd_it + 1) >> 1) & 1, abort)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+            issue_s((qd_it + 1) & 1);
+          }
           first = false;
+          ok = more;
         }
         if (failed) break;
         mma_commit(bar(KB_KV_EMPTY));
@@ -532,9 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (failed) raise_abort(abort, 0x200);
     }
   } else {
-    // ------------------------------------------------------------ element-wise (warps 0-3)
-    const int r = threadIdx.x;  // key of the tile == TMEM lane
-    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ element-wise (warps 0-7)
+    const int wg = warp >> 2;                    // query-row half of this warpgroup
+    const int r = (warp & 3) * 32 + lane;        // key of the tile == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t qd_it = 0, g_it = 0, unit_it = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
@@ -549,42 +597,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           failed = true;
           break;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_SP_FULL), g_it & 1, abort))) { failed = true; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_SP_FULL), qd_it & 1, abort))) { failed = true; break; }
         tc_fence_after();
-        const float* rd = rowdata + (qd_it & 1) * 256;
+        const float* rd = rowdata + (qd_it & 1) * 256 + wg * 64;
         // row c (token t0 + c % tt) sees this key iff the token index i = c % tt
         // lies in [i_lo, i_hi)
         const bool key_ok = key >= q.be.k_lo && key < q.be.k_hi;
         const int i_lo = q.be.causal ? max(0, key - q.t0) : 0;
         const int i_hi = key_ok ? min(tt, q.be.q_hi - q.t0) : 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t sv[32], dv[32], pp[16], dd[16];
-          tmem_ld32(tmem + lb + K_T_S + c * 32, sv);
-          tmem_ld32(tmem + lb + K_T_DP + c * 32, dv);
+          tmem_ld32(tmem + lb + K_T_S + wg * 64 + c * 32, sv);
+          tmem_ld32(tmem + lb + K_T_DP + wg * 64 + c * 32, dv);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const int col = c * 32 + i;
-            const int i0 = col & (tt - 1), i1 = (col + 1) & (tt - 1);
-            const float p0 = (i0 >= i_lo && i0 < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i]), p.sl2, -rd[col])) : 0.f;
+            const int col = c * 32 + i;  // within this half
+            const int i0 = (wg * 64 + col) & (tt - 1), i1 = (wg * 64 + col + 1) & (tt - 1);
+            const float p0 =
+                (i0 >= i_lo && i0 < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i]), p.sl2, -rd[col])) : 0.f;
             const float p1 =
                 (i1 >= i_lo && i1 < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.sl2, -rd[col + 1])) : 0.f;
             pp[i >> 1] = pack_bf16x2(p0, p1);
             dd[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[i]) - rd[128 + col]),
                                      p1 * (__uint_as_float(dv[i + 1]) - rd[128 + col + 1]));
           }
-          // P^T and dS^T as bf16 pairs over columns already read
-          tmem_st16(tmem + lb + K_T_S + c * 16, pp);
-          tmem_st16(tmem + lb + K_T_DP + c * 16, dd);
+          // P^T and dS^T as bf16 pairs over this half's columns, already read
+          tmem_st16(tmem + lb + K_T_S + wg * 64 + c * 16, pp);
+          tmem_st16(tmem + lb + K_T_DP + wg * 64 + c * 16, dd);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KB_PDS_FULL));
+        if (lane == 0) mbar_arrive(bar(KB_PDS_FULL + wg));
       }
       if (failed) break;
-      // epilogue: dV and dK of this key
+      // epilogue: this warpgroup's half of the key's dV and dK
       if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_ACC_DONE), unit_it & 1, abort))) { failed = true; break; }
       tc_fence_after();
       const bool valid = r < it.k_len;
@@ -592,14 +641,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int part = 0; part < 2; ++part) {
         __nv_bfloat16* out = part == 0 ? p.dv : p.dk;
         const float mul = part == 0 ? 1.f : p.scale;
-        const uint32_t col0 = part == 0 ? K_T_DV : K_T_DK;
+        const uint32_t col0 = (part == 0 ? K_T_DV : K_T_DK) + wg * 64;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lb + col0 + c * 32, v);
           tmem_wait_ld();
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(key) * p.Hkv + g) * kHeadDim + c * 32);
+            uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(key) * p.Hkv + g) * kHeadDim + wg * 64 +
+                                                  c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * mul, __uint_as_float(v[8 * i + 1]) * mul),
