@@ -160,6 +160,20 @@ PADOC_API int padoc_kv_append(padoc_kv_pool* pool, int32_t seq, const void* k, c
  * a partly used last block included).  0 <= fork_len <= length(parent). */
 PADOC_API int padoc_kv_fork(padoc_kv_pool* pool, int32_t parent, int32_t fork_len, int32_t* child);
 
+/* Grows seq's own blocks so that n_tokens more tokens fit after its current
+ * length (all or nothing: PADOC_ERR_OOM changes nothing).  Host bookkeeping
+ * only; a later append or commit of up to n_tokens then needs no block. */
+PADOC_API int padoc_kv_reserve(padoc_kv_pool* pool, int32_t seq, int32_t n_tokens);
+/* Marks n tokens after seq's current length as written, for callers that
+ * write K/V into the reserved slots themselves (a prefill into the pool's
+ * blocks through the block table).  The slots must already be reserved;
+ * otherwise PADOC_ERR_INVALID.  Host bookkeeping only. */
+PADOC_API int padoc_kv_advance(padoc_kv_pool* pool, int32_t seq, int32_t n);
+
+/* Gives back seq's own blocks past the ones its current length uses (the
+ * unused tail of a reservation); refcounts drop as in padoc_kv_release. */
+PADOC_API int padoc_kv_trim(padoc_kv_pool* pool, int32_t seq);
+
 /* Drops the sequence: refcount - 1 on each of its blocks, blocks at 0 return
  * to the free list, the sequence id becomes reusable. */
 PADOC_API int padoc_kv_release(padoc_kv_pool* pool, int32_t seq);
@@ -384,6 +398,80 @@ PADOC_API int padoc_draft_trie_batch(const padoc_draft_index* const* index, int3
                                      const int32_t* accepted, const int32_t* acc_offsets, int32_t max_nodes,
                                      int32_t max_depth, int32_t* tokens, int32_t* parents, int32_t* q_offsets,
                                      uint16_t* bits);
+
+/* ------------------------------------------------------------------------
+ * Branch scheduler (HPD-Parsing, inference workflow, Algorithm 1).  Host
+ * code over the KV pool; the model step (draft, verify, accept, commit) is
+ * the caller's, between padoc_sched_schedule and padoc_sched_update.
+ *   - Waiting requests are ordered first-come-first-served by keys: a child
+ *     (content) branch (0, arrival(parent), -m, arrival(child)) with m the
+ *     number of children its parent had spawned before it; a main (layout)
+ *     request (1, arrival); ties by request id.
+ *   - A main request is admitted only while pool occupancy (blocks in use /
+ *     pool blocks) <= tau and fewer than n_max requests are active; child
+ *     branches bypass that gate.  A child is ready once its parent is
+ *     resident with the tokens before the <FORK> that spawned it cached.  A request the
+ *     pool cannot hold now keeps its place; the scan goes on.
+ *   - Each step first reserves, for every active branch, room for its
+ *     cached tokens plus window + 1 (the anchor and the drafted tokens); when
+ *     the pool runs short the youngest active request (latest arrival, then
+ *     highest id) is preempted: its KV is released and it waits to be
+ *     rebuilt.  Requests preempted in a step are not readmitted in it.
+ *   - A branch's token stream is its prefix (the prompt; for a child, the
+ *     parent's tokens before the <FORK>) and its output.  Every token but
+ *     the newest is cached; the newest is the next step's anchor.  A child's
+ *     output starts with child_token.  Only main requests fork.
+ *   - A branch ends at eos_token or after max_len output tokens.  Its
+ *     sequence is released when it and all its children have ended; a main
+ *     request's output then interleaves each child's output after the <FORK>
+ *     that spawned it.
+ * The scheduler owns the pool sequences of its requests.  After admission
+ * the caller rebuilds the cached tokens of each admitted request (the
+ * request's sequence already counts them); after each step the caller
+ * commits the old anchor and the accepted tokens but the newest
+ * (padoc_kv_commit, or its own writes) before padoc_sched_update. */
+typedef struct {
+  float tau;            /* KV occupancy threshold in [0, 1] for admitting main requests */
+  int32_t n_max;        /* cap on active requests for admitting main requests */
+  int32_t window;       /* draft window K in [0, 15]: K + 1 query rows per branch and step */
+  int32_t max_len;      /* output tokens after which a branch ends (8000 in HPD-Parsing) */
+  int32_t fork_token;   /* <FORK> */
+  int32_t child_token;  /* <CHILD>: first token of a child branch */
+  int32_t eos_token;
+} padoc_sched_config;
+typedef struct padoc_sched padoc_sched;
+/* One step's decisions.  The caller provides arrays of capacity cap
+ * (branch_offsets cap + 1); the batch fields form a padoc_decode_batch
+ * (page_seq, branch_offsets, branch_seq = active_seq). */
+typedef struct {
+  int32_t cap;
+  int32_t n_admitted, n_preempted, n_active, n_pages;
+  int32_t* admitted;        /* request ids admitted this step (their cached tokens need rebuilding) */
+  int32_t* preempted;       /* request ids preempted this step */
+  int32_t* active;          /* active request ids, grouped by page, key order inside a page */
+  int32_t* active_seq;      /* their pool sequences */
+  int32_t* page_seq;        /* per page: the sequence holding the shared prefix */
+  int32_t* branch_offsets;  /* [n_pages + 1] */
+} padoc_sched_step;
+PADOC_API int padoc_sched_create(padoc_kv_pool* pool, const padoc_sched_config* cfg, padoc_sched** out);
+/* Releases the pool sequences the scheduler still holds. */
+PADOC_API int padoc_sched_destroy(padoc_sched* sched);
+/* A main request with prompt_len >= 1 tokens (its last token is the first anchor). */
+PADOC_API int padoc_sched_submit(padoc_sched* sched, int32_t prompt_len, int64_t arrival, int32_t* request);
+PADOC_API int padoc_sched_schedule(padoc_sched* sched, padoc_sched_step* step);
+/* The verified tokens of each listed running request (n_acc drafted tokens
+ * plus the free token, at least one): request [n], token_offsets [n + 1],
+ * tokens.  Processed in the given order; now is the arrival time of the
+ * children spawned. */
+PADOC_API int padoc_sched_update(padoc_sched* sched, int64_t now, int32_t n, const int32_t* request,
+                                 const int32_t* token_offsets, const int32_t* tokens);
+/* state: 0 waiting, 1 running, 2 ended (children pending), 3 done. */
+PADOC_API int padoc_sched_request(const padoc_sched* sched, int32_t request, int32_t* state, int32_t* seq,
+                                  int32_t* parent, int64_t* n_out);
+/* The interleaved output of a done main request; tokens may be NULL to
+ * query the length. */
+PADOC_API int padoc_sched_output(const padoc_sched* sched, int32_t request, int32_t* tokens, int64_t cap,
+                                 int64_t* n);
 
 /* Critical-path depths of one page (PaDoc, theoretical speedup):
  * d_seq = l(B_1:N) + sum_k l(Y_k);  d_tree = max_k [l(B<=k) + l(Y_k)]. */

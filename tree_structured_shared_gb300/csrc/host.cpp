@@ -712,6 +712,51 @@ extern "C" int padoc_kv_fork(padoc_kv_pool* pool, int32_t parent, int32_t fork_l
   return PADOC_OK;
 }
 
+extern "C" int padoc_kv_reserve(padoc_kv_pool* pool, int32_t seq, int32_t n_tokens) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_reserve: null pool");
+  if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_reserve: %d is not a live sequence", seq);
+  if (n_tokens < 0) return fail(PADOC_ERR_INVALID, "kv_reserve: n_tokens < 0");
+  Seq& s = pool->seqs[seq];
+  const int64_t need = (static_cast<int64_t>(s.len - s.fork_len) + n_tokens + pool->bs - 1) / pool->bs;
+  const int64_t have = pool->own_blocks(s);
+  if (s.n_shared + need > pool->max_bps)
+    return fail(PADOC_ERR_INVALID, "kv_reserve: sequence would exceed max_blocks_per_seq");
+  if (need > have) {
+    std::vector<int32_t> extra;
+    PADOC_TRY({
+      if (!pool->take_blocks(static_cast<int32_t>(need - have), &extra))
+        return fail(PADOC_ERR_OOM, "kv_reserve: out of blocks");
+      s.blocks.insert(s.blocks.end(), extra.begin(), extra.end());
+      pool->mark(seq);
+    });
+  }
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_advance(padoc_kv_pool* pool, int32_t seq, int32_t n) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_advance: null pool");
+  if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_advance: %d is not a live sequence", seq);
+  if (n < 0) return fail(PADOC_ERR_INVALID, "kv_advance: n < 0");
+  Seq& s = pool->seqs[seq];
+  if (static_cast<int64_t>(s.len - s.fork_len) + n > static_cast<int64_t>(pool->own_blocks(s)) * pool->bs)
+    return fail(PADOC_ERR_INVALID, "kv_advance: %d tokens exceed the reserved slots", n);
+  s.len += n;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_kv_trim(padoc_kv_pool* pool, int32_t seq) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "kv_trim: null pool");
+  if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_trim: %d is not a live sequence", seq);
+  Seq& s = pool->seqs[seq];
+  const size_t keep = static_cast<size_t>(s.n_shared) + (s.len - s.fork_len + pool->bs - 1) / pool->bs;
+  if (s.blocks.size() > keep) {
+    for (size_t i = keep; i < s.blocks.size(); ++i) pool->drop_block(s.blocks[i]);
+    s.blocks.resize(keep);
+    pool->mark(seq);
+  }
+  return PADOC_OK;
+}
+
 extern "C" int padoc_kv_release(padoc_kv_pool* pool, int32_t seq) {
   if (!pool) return fail(PADOC_ERR_INVALID, "kv_release: null pool");
   if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_release: %d is not a live sequence", seq);
@@ -1228,6 +1273,7 @@ int set_error(int code, const char* fmt, ...) {
   return fail(code, "%s", buf);
 }
 bool pool_has_device_table(const padoc_kv_pool* pool) { return pool && pool->d_table; }
+int32_t pool_num_blocks(const padoc_kv_pool* pool) { return pool ? pool->nb : 0; }
 }  // namespace padoc
 
 extern "C" int padoc_verify_accept(const void* logits, int32_t nq, int32_t vocab, const int32_t* tokens,

@@ -168,6 +168,7 @@ int num_sms();
 
 // Records an error message for padoc_last_error() and returns code.
 int set_error(int code, const char* fmt, ...);
+int32_t pool_num_blocks(const padoc_kv_pool* pool);
 // True once the pool's device block table exists (padoc_kv_pool_sync ran).
 bool pool_has_device_table(const padoc_kv_pool* pool);
 

@@ -31,7 +31,9 @@ EXPORTED = [
     "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free", "padoc_branch_decode_noalloc",
     "padoc_verify_accept", "padoc_kv_commit", "padoc_draft_index_create", "padoc_draft_index_free",
     "padoc_draft_trie", "padoc_draft_trie_batch", "padoc_tree_attn_varlen_bwd_ws_size",
-    "padoc_tree_attn_varlen_bwd", "padoc_tree_desc_bwd_plan",
+    "padoc_tree_attn_varlen_bwd", "padoc_tree_desc_bwd_plan", "padoc_kv_reserve", "padoc_kv_advance", "padoc_kv_trim",
+    "padoc_sched_create", "padoc_sched_destroy", "padoc_sched_submit", "padoc_sched_schedule", "padoc_sched_update",
+    "padoc_sched_request", "padoc_sched_output",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -46,6 +48,18 @@ class TreeSpec(C.Structure):
     _fields_ = [("n_pages", C.c_int32), ("prefix_len", C.POINTER(C.c_int32)),
                 ("n_regions", C.POINTER(C.c_int32)), ("layout_len", C.POINTER(C.c_int32)),
                 ("content_len", C.POINTER(C.c_int32)), ("order", C.c_int32)]
+
+
+class SchedConfig(C.Structure):
+    _fields_ = [("tau", C.c_float), ("n_max", C.c_int32), ("window", C.c_int32), ("max_len", C.c_int32),
+                ("fork_token", C.c_int32), ("child_token", C.c_int32), ("eos_token", C.c_int32)]
+
+
+class SchedStep(C.Structure):
+    _fields_ = [("cap", C.c_int32), ("n_admitted", C.c_int32), ("n_preempted", C.c_int32), ("n_active", C.c_int32),
+                ("n_pages", C.c_int32), ("admitted", C.POINTER(C.c_int32)), ("preempted", C.POINTER(C.c_int32)),
+                ("active", C.POINTER(C.c_int32)), ("active_seq", C.POINTER(C.c_int32)),
+                ("page_seq", C.POINTER(C.c_int32)), ("branch_offsets", C.POINTER(C.c_int32))]
 
 
 class DecodeBatch(C.Structure):
@@ -102,6 +116,16 @@ def lib() -> C.CDLL:
                                                       vp]),
             "padoc_verify_accept": (C.c_int, [vp, i32, i32, vp, vp, vp, i32, i32, f32, vp, vp, vp, vp]),
             "padoc_kv_commit": (C.c_int, [vp, i32, p32, p32, p32, i32, vp, vp, vp, C.c_size_t, vp]),
+            "padoc_kv_reserve": (C.c_int, [vp, i32, i32]),
+            "padoc_kv_advance": (C.c_int, [vp, i32, i32]),
+            "padoc_kv_trim": (C.c_int, [vp, i32]),
+            "padoc_sched_create": (C.c_int, [vp, C.POINTER(SchedConfig), C.POINTER(vp)]),
+            "padoc_sched_destroy": (C.c_int, [vp]),
+            "padoc_sched_submit": (C.c_int, [vp, i32, i64, p32]),
+            "padoc_sched_schedule": (C.c_int, [vp, C.POINTER(SchedStep)]),
+            "padoc_sched_update": (C.c_int, [vp, i64, i32, p32, p32, p32]),
+            "padoc_sched_request": (C.c_int, [vp, i32, p32, p32, p32, p64]),
+            "padoc_sched_output": (C.c_int, [vp, i32, p32, i64, p64]),
             "padoc_tree_attn_varlen_bwd_ws_size": (C.c_int, [vp, i32, C.POINTER(C.c_size_t)]),
             "padoc_tree_attn_varlen_bwd": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                      f32, vp, C.c_size_t, vp]),
@@ -286,6 +310,15 @@ class KVPool:
     def sync(self, stream=None):
         _check(lib().padoc_kv_pool_sync(self.handle, _stream(stream)))
 
+    def reserve(self, seq: int, n_tokens: int):
+        _check(lib().padoc_kv_reserve(self.handle, seq, n_tokens))
+
+    def advance(self, seq: int, n: int):
+        _check(lib().padoc_kv_advance(self.handle, seq, n))
+
+    def trim(self, seq: int):
+        _check(lib().padoc_kv_trim(self.handle, seq))
+
     def commit(self, seqs: Sequence[int], row_offsets: Sequence[int], rows: Sequence[int], n_src_rows: int,
                k_new, v_new, ws, ws_bytes: int, stream=None):
         """padoc_kv_commit: appends rows[row_offsets[i]:row_offsets[i+1]] of
@@ -400,6 +433,70 @@ def draft_trie_batch(indexes: Sequence[DraftIndex], accepted: Sequence[Sequence[
                                         _p32(q), bits.ctypes.data_as(C.POINTER(C.c_uint16))))
     nq = int(q[-1])
     return t[:nq], p[:nq], q, bits[:nq]
+
+
+class Scheduler:
+    """The branch scheduler over a KV pool (padoc_sched_*)."""
+
+    STATES = ("waiting", "running", "ended", "done")
+
+    def __init__(self, pool: "KVPool", tau: float, n_max: int, window: int, max_len: int, fork_token: int,
+                 child_token: int, eos_token: int, cap: int = 4096):
+        self.pool = pool
+        cfg = SchedConfig(tau, n_max, window, max_len, fork_token, child_token, eos_token)
+        h = C.c_void_p()
+        _check(lib().padoc_sched_create(pool.handle, C.byref(cfg), C.byref(h)))
+        self.handle = h
+        self.cap = cap
+        self._bufs = [np.zeros(cap + 1, np.int32) for _ in range(6)]
+
+    def submit(self, prompt_len: int, arrival: int) -> int:
+        r = C.c_int32()
+        _check(lib().padoc_sched_submit(self.handle, prompt_len, arrival, C.byref(r)))
+        return r.value
+
+    def schedule(self):
+        """admitted, preempted, and the batch as [(page_seq, [(request, seq), ...]), ...]."""
+        b = self._bufs
+        st = SchedStep(self.cap, 0, 0, 0, 0, *[_p32(x) for x in b])
+        _check(lib().padoc_sched_schedule(self.handle, C.byref(st)))
+        pages = []
+        for p in range(st.n_pages):
+            lo, hi = b[5][p], b[5][p + 1]
+            pages.append((int(b[4][p]), [(int(b[2][i]), int(b[3][i])) for i in range(lo, hi)]))
+        return b[0][: st.n_admitted].tolist(), b[1][: st.n_preempted].tolist(), pages
+
+    def update(self, now: int, accepted):
+        """accepted: [(request, [tokens...]), ...] in processing order."""
+        req = _i32([r for r, _ in accepted] or [0])
+        off = np.zeros(len(accepted) + 1, np.int32)
+        off[1:] = np.cumsum([len(t) for _, t in accepted])
+        toks = _i32([t for _, ts in accepted for t in ts] or [0])
+        _check(lib().padoc_sched_update(self.handle, now, len(accepted), _p32(req), _p32(off), _p32(toks)))
+
+    def request(self, rid: int):
+        st, seq, par = C.c_int32(), C.c_int32(), C.c_int32()
+        n = C.c_int64()
+        _check(lib().padoc_sched_request(self.handle, rid, C.byref(st), C.byref(seq), C.byref(par), C.byref(n)))
+        return {"state": self.STATES[st.value], "seq": seq.value, "parent": par.value, "n_out": n.value}
+
+    def output(self, rid: int):
+        n = C.c_int64()
+        _check(lib().padoc_sched_output(self.handle, rid, None, 0, C.byref(n)))
+        out = np.zeros(max(n.value, 1), np.int32)
+        _check(lib().padoc_sched_output(self.handle, rid, _p32(out), len(out), C.byref(n)))
+        return out[: n.value].tolist()
+
+    def destroy(self):
+        if self.handle:
+            lib().padoc_sched_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
 
 
 class DecodePlan:
