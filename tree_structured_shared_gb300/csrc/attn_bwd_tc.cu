@@ -48,6 +48,18 @@ constexpr int kHalf = 16384;  // one 64-column half of a 128-row bf16 tile
 constexpr int kTile = 2 * kHalf;
 constexpr float kLog2e = 1.44269504088896340736f;
 
+// Descriptors of the 16-wide K steps of a 128-byte-swizzled tile, as
+// offsets from the tile's base descriptor (the start address field holds the
+// address / 16, and no step carries out of it): K-major operands step 32
+// bytes inside a 64-column half and then to the other half; MN-major
+// operands step 16 rows of 128 bytes.
+__device__ __forceinline__ uint64_t kmajor_step(uint64_t base, int kk) {
+  return base + static_cast<uint64_t>(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t mnmajor_step(uint64_t base, int kk) {
+  return base + static_cast<uint64_t>(kk * (2048 >> 4));
+}
+
 __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned site) {
   *abort = 1;
   atomicOr(&g_bwd_err, site);
@@ -227,19 +239,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);   // B MN-major
       uint32_t kv_it = 0, g_it = 0, unit_it = 0;
       bool failed = false;
+      // base descriptors: Q and dO (K-major), K and V of each stage (K-major), K as MN-major B
+      const uint64_t d_q = sdesc_sw128(sbase + Q_SM_Q, 16, 1024), d_do = sdesc_sw128(sbase + Q_SM_DO, 16, 1024);
+      const uint64_t d_k0 = sdesc_sw128(sbase + Q_SM_K, 16, 1024), d_k1 = sdesc_sw128(sbase + Q_SM_K + kTile, 16, 1024);
+      const uint64_t d_v0 = sdesc_sw128(sbase + Q_SM_V, 16, 1024), d_v1 = sdesc_sw128(sbase + Q_SM_V + kTile, 16, 1024);
+      const uint64_t d_kmn0 = sdesc_sw128(sbase + Q_SM_K, kHalf, 1024);
+      const uint64_t d_kmn1 = sdesc_sw128(sbase + Q_SM_K + kTile, kHalf, 1024);
       auto issue_dq = [&](uint32_t tile_it, bool first, bool last) -> bool {
         // dQ += dS K for tile tile_it (dS in TMEM, K of its stage as MN-major
         // B), one key half at a time as each warpgroup finishes its dS
         if (first && !mbar_wait_relaxed(bar(QB_ACC_FREE), (unit_it & 1) ^ 1, abort)) return false;
         const int st = tile_it & 1;
-        const uint32_t ka = sbase + Q_SM_K + st * kTile;
+        const uint64_t kd = st ? d_kmn1 : d_kmn0;
         for (int half = 0; half < 2; ++half) {
           if (!mbar_wait_relaxed(bar(QB_DS_FULL + half), tile_it & 1, abort)) return false;
           tc_fence_after();
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = half * 4 + k4;
-            mma_bf16_ts(tmem + Q_T_DQ, tmem + Q_T_DS + kk * 8, sdesc_sw128(ka + kk * 2048, kHalf, 1024), id_mn,
+            mma_bf16_ts(tmem + Q_T_DQ, tmem + Q_T_DS + kk * 8, mnmajor_step(kd, kk), id_mn,
                         (!first || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(QB_DQ_DONE + half));
@@ -253,27 +271,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = key_count(p, w);
         if (n == 0) continue;
         if (!mbar_wait_relaxed(bar(QB_QD_FULL), unit_it & 1, abort)) { failed = true; break; }
-        const uint32_t qa = sbase + Q_SM_Q, da = sbase + Q_SM_DO;
         for (int j = 0; j < n; ++j, ++kv_it, ++g_it) {
           const int st = kv_it & 1;
           if (!mbar_wait_relaxed(bar(QB_KV_FULL + st), (kv_it >> 1) & 1, abort)) { failed = true; break; }
-          const uint32_t ka = sbase + Q_SM_K + st * kTile, va = sbase + Q_SM_V + st * kTile;
+          const uint64_t dk = st ? d_k1 : d_k0, dv = st ? d_v1 : d_v0;
           // S and dP go over columns both warpgroups have read (they compute the
           // previous tile's dS from registers meanwhile)
           if (g_it > 0 && !mbar_wait_relaxed(bar(QB_RD), (g_it - 1) & 1, abort)) { failed = true; break; }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            mma_bf16_ss(tmem + Q_T_S, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), id_kk,
-                        kk > 0);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + Q_T_S, kmajor_step(d_q, kk), kmajor_step(dk, kk), id_kk, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            mma_bf16_ss(tmem + Q_T_DP, sdesc_sw128(da + off, 16, 1024), sdesc_sw128(va + off, 16, 1024), id_kk,
-                        kk > 0);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + Q_T_DP, kmajor_step(d_do, kk), kmajor_step(dv, kk), id_kk, kk > 0);
           mma_commit(bar(QB_SP_FULL));
           if (j == n - 1) mma_commit(bar(QB_QD_EMPTY));
           if (j > 0 && !issue_dq(g_it - 1, j == 1, false)) { failed = true; break; }
@@ -320,15 +331,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(QB_RD));
         uint32_t pk[32];
+        if (__all_sync(0xffffffffu, vis >= 64)) {  // no masked column in this half for the warp
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int col = c * 32 + i;
-            const float p0 = col < vis ? fast_exp2(fmaf(__uint_as_float(sv[c][i]), p.sl2, -lse2)) : 0.f;
-            const float p1 = col + 1 < vis ? fast_exp2(fmaf(__uint_as_float(sv[c][i + 1]), p.sl2, -lse2)) : 0.f;
-            pk[col >> 1] =
-                pack_bf16x2(p0 * (__uint_as_float(dv[c][i]) - Dr), p1 * (__uint_as_float(dv[c][i + 1]) - Dr));
+            for (int i = 0; i < 32; i += 2) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c][i]), p.sl2, -lse2));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c][i + 1]), p.sl2, -lse2));
+              pk[(c * 32 + i) >> 1] =
+                  pack_bf16x2(p0 * (__uint_as_float(dv[c][i]) - Dr), p1 * (__uint_as_float(dv[c][i + 1]) - Dr));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int col = c * 32 + i;
+              const float p0 = col < vis ? fast_exp2(fmaf(__uint_as_float(sv[c][i]), p.sl2, -lse2)) : 0.f;
+              const float p1 = col + 1 < vis ? fast_exp2(fmaf(__uint_as_float(sv[c][i + 1]), p.sl2, -lse2)) : 0.f;
+              pk[col >> 1] =
+                  pack_bf16x2(p0 * (__uint_as_float(dv[c][i]) - Dr), p1 * (__uint_as_float(dv[c][i + 1]) - Dr));
+            }
           }
         }
         // dS goes over the previous tile's dS once that tile's dQ has read it
@@ -510,22 +534,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);
       uint32_t qd_it = 0, unit_it = 0;
       bool failed = false;
-      const uint32_t ka = sbase + K_SM_K, va = sbase + K_SM_V;
+      // base descriptors: K and V (K-major A), Q and dO of each stage as
+      // K-major B (for S^T, dP^T) and as MN-major B (for dK, dV)
+      const uint64_t d_k = sdesc_sw128(sbase + K_SM_K, 16, 1024), d_v = sdesc_sw128(sbase + K_SM_V, 16, 1024);
+      uint64_t d_q[2], d_do[2], d_qmn[2], d_domn[2];
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {
+        const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile;
+        d_q[st] = sdesc_sw128(qa, 16, 1024);
+        d_do[st] = sdesc_sw128(qa + kTile, 16, 1024);
+        d_qmn[st] = sdesc_sw128(qa, kHalf, 1024);
+        d_domn[st] = sdesc_sw128(qa + kTile, kHalf, 1024);
+      }
       // S^T = K Q^T and dP^T = V dO^T for the tile in stage st
       auto issue_s = [&](int st) {
-        const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile, da = qa + kTile;
+        const uint64_t dq = st ? d_q[1] : d_q[0], ddo = st ? d_do[1] : d_do[0];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          mma_bf16_ss(tmem + K_T_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), id_kk,
-                      kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk) mma_bf16_ss(tmem + K_T_S, kmajor_step(d_k, kk), kmajor_step(dq, kk), id_kk, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          mma_bf16_ss(tmem + K_T_DP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), id_kk,
-                      kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tmem + K_T_DP, kmajor_step(d_v, kk), kmajor_step(ddo, kk), id_kk, kk > 0);
         mma_commit(bar(KB_SP_FULL));
       };
       for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
@@ -539,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool first = true;
         for (bool ok = true; ok; ++qd_it) {
           const int st = qd_it & 1;
-          const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile, da = qa + kTile;
+          const uint64_t dqm = st ? d_qmn[1] : d_qmn[0], ddom = st ? d_domn[1] : d_domn[0];
           const bool more = q_next(p, q);
           if (first && !mbar_wait_relaxed(bar(KB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
           for (int half = 0; half < 2; ++half) {
@@ -550,14 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
               const int kk = half * 4 + k4;
-              mma_bf16_ts(tmem + K_T_DV, tmem + K_T_S + half * 64 + k4 * 8, sdesc_sw128(da + kk * 2048, kHalf, 1024),
-                          id_mn, (!first || kk > 0) ? 1u : 0u);
+              mma_bf16_ts(tmem + K_T_DV, tmem + K_T_S + half * 64 + k4 * 8, mnmajor_step(ddom, kk), id_mn,
+                          (!first || kk > 0) ? 1u : 0u);
             }
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
               const int kk = half * 4 + k4;
-              mma_bf16_ts(tmem + K_T_DK, tmem + K_T_DP + half * 64 + k4 * 8, sdesc_sw128(qa + kk * 2048, kHalf, 1024),
-                          id_mn, (!first || kk > 0) ? 1u : 0u);
+              mma_bf16_ts(tmem + K_T_DK, tmem + K_T_DP + half * 64 + k4 * 8, mnmajor_step(dqm, kk), id_mn,
+                          (!first || kk > 0) ? 1u : 0u);
             }
           }
           if (failed) break;
@@ -609,23 +637,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool key_ok = key >= q.be.k_lo && key < q.be.k_hi;
         const int i_lo = q.be.causal ? max(0, key - q.t0) : 0;
         const int i_hi = key_ok ? min(tt, q.be.q_hi - q.t0) : 0;
+        // every row of the tile sees every key of the warp: no masks
+        const bool all_visible = __all_sync(0xffffffffu, i_lo == 0 && i_hi == tt);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sv[32], dv[32], pp[16], dd[16];
           tmem_ld32(tmem + lb + K_T_S + wg * 64 + c * 32, sv);
           tmem_ld32(tmem + lb + K_T_DP + wg * 64 + c * 32, dv);
           tmem_wait_ld();
+          const float4* l4 = reinterpret_cast<const float4*>(rd) + c * 8;       // LSE (log2) of the chunk's rows
+          const float4* d4 = reinterpret_cast<const float4*>(rd + 128) + c * 8;  // D of the chunk's rows
+          if (all_visible) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int col = c * 32 + i;  // within this half
-            const int i0 = (wg * 64 + col) & (tt - 1), i1 = (wg * 64 + col + 1) & (tt - 1);
-            const float p0 =
-                (i0 >= i_lo && i0 < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i]), p.sl2, -rd[col])) : 0.f;
-            const float p1 =
-                (i1 >= i_lo && i1 < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.sl2, -rd[col + 1])) : 0.f;
-            pp[i >> 1] = pack_bf16x2(p0, p1);
-            dd[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[i]) - rd[128 + col]),
-                                     p1 * (__uint_as_float(dv[i + 1]) - rd[128 + col + 1]));
+            for (int i = 0; i < 32; i += 4) {
+              const float4 l = l4[i >> 2], dl = d4[i >> 2];
+              const float p0 = fast_exp2(fmaf(__uint_as_float(sv[i + 0]), p.sl2, -l.x));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.sl2, -l.y));
+              const float p2 = fast_exp2(fmaf(__uint_as_float(sv[i + 2]), p.sl2, -l.z));
+              const float p3 = fast_exp2(fmaf(__uint_as_float(sv[i + 3]), p.sl2, -l.w));
+              pp[(i >> 1) + 0] = pack_bf16x2(p0, p1);
+              pp[(i >> 1) + 1] = pack_bf16x2(p2, p3);
+              dd[(i >> 1) + 0] = pack_bf16x2(p0 * (__uint_as_float(dv[i + 0]) - dl.x), p1 * (__uint_as_float(dv[i + 1]) - dl.y));
+              dd[(i >> 1) + 1] = pack_bf16x2(p2 * (__uint_as_float(dv[i + 2]) - dl.z), p3 * (__uint_as_float(dv[i + 3]) - dl.w));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 l = l4[i >> 2], dl = d4[i >> 2];
+              const float lv[4] = {l.x, l.y, l.z, l.w}, dd4[4] = {dl.x, dl.y, dl.z, dl.w};
+              float pv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int ie = (wg * 64 + c * 32 + i + e) & (tt - 1);
+                pv[e] = (ie >= i_lo && ie < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i + e]), p.sl2, -lv[e])) : 0.f;
+              }
+              pp[(i >> 1) + 0] = pack_bf16x2(pv[0], pv[1]);
+              pp[(i >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
+              dd[(i >> 1) + 0] =
+                  pack_bf16x2(pv[0] * (__uint_as_float(dv[i + 0]) - dd4[0]), pv[1] * (__uint_as_float(dv[i + 1]) - dd4[1]));
+              dd[(i >> 1) + 1] =
+                  pack_bf16x2(pv[2] * (__uint_as_float(dv[i + 2]) - dd4[2]), pv[3] * (__uint_as_float(dv[i + 3]) - dd4[3]));
+            }
           }
           // P^T and dS^T as bf16 pairs over this half's columns, already read
           tmem_st16(tmem + lb + K_T_S + wg * 64 + c * 16, pp);
