@@ -498,13 +498,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         float s[128];
         {
-          uint32_t v[32];
+          // all four loads in flight before one wait
+          uint32_t v0[32], v1[32], v2[32], v3[32];
+          tmem_ld32(tmem + lane_base + sb * 128 + 0, v0);
+          tmem_ld32(tmem + lane_base + sb * 128 + 32, v1);
+          tmem_ld32(tmem + lane_base + sb * 128 + 64, v2);
+          tmem_ld32(tmem + lane_base + sb * 128 + 96, v3);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tmem + lane_base + sb * 128 + c * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 32; ++i) {
+            s[i] = __uint_as_float(v0[i]);
+            s[32 + i] = __uint_as_float(v1[i]);
+            s[64 + i] = __uint_as_float(v2[i]);
+            s[96 + i] = __uint_as_float(v3[i]);
           }
         }
         ++s_it;
@@ -537,8 +543,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) m8[i] = s[i];
 #pragma unroll
-          for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
-          tmax = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int c = 8; c < 120; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m8[i] = max3f(m8[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[120 + i]);
+          tmax = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
         const float mt = tmax * p.sl2;
         const bool grow = mt > m_run + kRescaleThreshold;
@@ -549,12 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         {
-          float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          // x = s * sl2 - m two lanes per instruction; the same partial sums
+          // (lane k of the row sum takes columns c with c % 8 == k)
+          const uint64_t sl2x2 = f2pack(p.sl2, p.sl2), negm = f2pack(-m_use, -m_use);
+          uint64_t l2[4] = {0, 0, 0, 0};
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            s[c] = fast_exp2(fmaf(s[c], p.sl2, -m_use));
-            l8[c & 7] += s[c];
+          for (int c = 0; c < 128; c += 2) {
+            float x0, x1;
+            f2unpack(fma2(f2pack(s[c], s[c + 1]), sl2x2, negm), x0, x1);
+            s[c] = fast_exp2(x0);
+            s[c + 1] = fast_exp2(x1);
+            l2[(c >> 1) & 3] = add2(l2[(c >> 1) & 3], f2pack(s[c], s[c + 1]));
           }
+          float l8[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) f2unpack(l2[k], l8[2 * k], l8[2 * k + 1]);
           l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         }
         // Every P V product completes one O_DONE phase; wait for each one in
