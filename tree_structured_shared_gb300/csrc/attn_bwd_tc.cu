@@ -331,15 +331,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(QB_RD));
         uint32_t pk[32];
+        const uint64_t sl2x2 = f2pack(p.sl2, p.sl2), negl2 = f2pack(-lse2, -lse2), d2 = f2pack(Dr, Dr);
         if (__all_sync(0xffffffffu, vis >= 64)) {  // no masked column in this half for the warp
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-              const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c][i]), p.sl2, -lse2));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c][i + 1]), p.sl2, -lse2));
-              pk[(c * 32 + i) >> 1] =
-                  pack_bf16x2(p0 * (__uint_as_float(dv[c][i]) - Dr), p1 * (__uint_as_float(dv[c][i + 1]) - Dr));
+              // two lanes per instruction: x = s * sl2 - LSE2, P = 2^x, dS = P (dP - D)
+              float x0, x1;
+              f2unpack(fma2(f2pack(__uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1])), sl2x2, negl2), x0, x1);
+              const uint64_t ds = mul2(f2pack(fast_exp2(x0), fast_exp2(x1)),
+                                       sub2(f2pack(__uint_as_float(dv[c][i]), __uint_as_float(dv[c][i + 1])), d2));
+              float a, b;
+              f2unpack(ds, a, b);
+              pk[(c * 32 + i) >> 1] = pack_bf16x2(a, b);
             }
           }
         } else {
@@ -639,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i_hi = key_ok ? min(tt, q.be.q_hi - q.t0) : 0;
         // every row of the tile sees every key of the warp: no masks
         const bool all_visible = __all_sync(0xffffffffu, i_lo == 0 && i_hi == tt);
+        const uint64_t sl2x2 = f2pack(p.sl2, p.sl2);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sv[32], dv[32], pp[16], dd[16];
@@ -651,14 +657,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               const float4 l = l4[i >> 2], dl = d4[i >> 2];
-              const float p0 = fast_exp2(fmaf(__uint_as_float(sv[i + 0]), p.sl2, -l.x));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(sv[i + 1]), p.sl2, -l.y));
-              const float p2 = fast_exp2(fmaf(__uint_as_float(sv[i + 2]), p.sl2, -l.z));
-              const float p3 = fast_exp2(fmaf(__uint_as_float(sv[i + 3]), p.sl2, -l.w));
-              pp[(i >> 1) + 0] = pack_bf16x2(p0, p1);
-              pp[(i >> 1) + 1] = pack_bf16x2(p2, p3);
-              dd[(i >> 1) + 0] = pack_bf16x2(p0 * (__uint_as_float(dv[i + 0]) - dl.x), p1 * (__uint_as_float(dv[i + 1]) - dl.y));
-              dd[(i >> 1) + 1] = pack_bf16x2(p2 * (__uint_as_float(dv[i + 2]) - dl.z), p3 * (__uint_as_float(dv[i + 3]) - dl.w));
+              // two lanes per instruction: x = s * sl2 - LSE2, P = 2^x, dS = P (dP - D)
+              float x0, x1, x2, x3;
+              f2unpack(fma2(f2pack(__uint_as_float(sv[i + 0]), __uint_as_float(sv[i + 1])), sl2x2, f2pack(-l.x, -l.y)), x0, x1);
+              f2unpack(fma2(f2pack(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), sl2x2, f2pack(-l.z, -l.w)), x2, x3);
+              const uint64_t p01 = f2pack(fast_exp2(x0), fast_exp2(x1)), p23 = f2pack(fast_exp2(x2), fast_exp2(x3));
+              const uint64_t d01 = mul2(p01, sub2(f2pack(__uint_as_float(dv[i + 0]), __uint_as_float(dv[i + 1])), f2pack(dl.x, dl.y)));
+              const uint64_t d23 = mul2(p23, sub2(f2pack(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2pack(dl.z, dl.w)));
+              float a, b;
+              f2unpack(p01, a, b);
+              pp[(i >> 1) + 0] = pack_bf16x2(a, b);
+              f2unpack(p23, a, b);
+              pp[(i >> 1) + 1] = pack_bf16x2(a, b);
+              f2unpack(d01, a, b);
+              dd[(i >> 1) + 0] = pack_bf16x2(a, b);
+              f2unpack(d23, a, b);
+              dd[(i >> 1) + 1] = pack_bf16x2(a, b);
             }
           } else {
 #pragma unroll
