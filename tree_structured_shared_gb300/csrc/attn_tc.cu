@@ -18,24 +18,25 @@
 //                with zero copy).  Writes normalised partial O and LSE.
 //
 // Roles (224 threads):
-//   warps 0-3  softmax: thread r owns TMEM lane r = query row r.  Copies its
-//              Q row into TMEM at the start of a unit.  Reads S from
-//              TMEM, masks, keeps the running max / sum, writes P (bf16 pairs)
-//              back over the S tile in TMEM, rescales O in TMEM when the max
-//              grows by more than 2^8, and runs the epilogue.
+//   warps 0-3  softmax: thread r owns TMEM lane r = query row r.  Reads S
+//              from TMEM, masks, keeps the running max / sum, writes P (bf16
+//              pairs) back over the S tile in TMEM, rescales O in TMEM when
+//              the max grows by more than 2^8, and runs the epilogue.
 //   warp 4     producer of Q and K tiles (TMA); decode: also stages the
 //              chunk's block ids in shared memory.
-//   warp 6     producer of V tiles (TMA).  K and V of a key tile share one
-//              ring stage and one full barrier, so the MMA thread waits once
-//              per tile for both.
-//   warp 5     MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
-//              tile, O += P V (P read from TMEM) into a TMEM accumulator.
+//   warp 6     producer of V tiles (TMA).
+//   warp 5     MMA issuer (one thread): S = Q K^T into one of three TMEM
+//              tiles, two key tiles ahead of the softmax, and O += P V (P read
+//              from TMEM) into a TMEM accumulator.
 //
-// TMEM: columns [0,128) and [128,256) hold S (then P), [256,384) hold O
-// (f32), [384,448) hold Q as bf16 pairs, so both MMAs read A from TMEM and
-// only K and V come from shared memory.
+// TMEM: columns [0,128), [128,256) and [256,384) hold S (then P), [384,512)
+// hold O (f32).  With three S tiles the S of tile j+2 needs only the P V of
+// tile j-1 to have been issued, so the softmax never waits for its next S.
+// K and V have rings of their own: a K stage is free once its S has run, a V
+// stage once its P V has, so each ring prefetches as far as its lifetime
+// allows.
 // Shared memory (1024-byte aligned, 128-byte swizzle, two 64-column halves):
-//   Q 32 KB | K 3 x 32 KB | V 3 x 32 KB (ring of 3 K/V stages) | barriers | block ids.
+//   Q 32 KB | K 3 x 32 KB | V 3 x 32 KB | barriers | block ids.
 // Every wait is bounded; a unit that times out raises the CTA abort flag, the
 // device error word, and all roles leave their loops.
 #include <cuda_bf16.h>
@@ -54,7 +55,8 @@ using namespace ptx;
 
 enum { MODE_FWD = 0, MODE_PREFIX = 1, MODE_OWN = 2 };
 
-constexpr int kStages = 3;  // K/V tile ring; stage s holds K and V of the same key tile
+constexpr int kStages = 3;  // K and V tile rings
+constexpr int kSBufs = 3;   // S / P tiles in tensor memory
 constexpr int kThreads = 224;
 constexpr int kHalf = 16384;  // bytes of one 64-column half of a 128-row tile
 constexpr int SM_Q = 0;
@@ -70,22 +72,22 @@ constexpr int kSmemBytes = SM_TOTAL + 1024;
 // barrier slots
 enum {
   B_Q_FULL = 0,
-  B_Q_EMPTY = 1,
-  B_KV_FULL = 2,   // +stage (3): K and V of the stage landed (one arrival per producer)
-  B_KV_EMPTY = 5,  // +stage (3): P V of the stage's tile completed
-  B_SPARE = 8,     // six unused slots
-  B_S_FULL = 14,  // +buffer (2)
-  B_P_FULL = 16,
-  B_O_DONE = 17,
-  B_O_FREE = 18,
-  B_IDS_READY = 19,  // prefix pass: the chunk's block ids are staged
-  B_IDS_FREE = 20,   // prefix pass: the V producer is done with them
-  B_QT_FULL = 21,    // softmax warps copied Q into tensor memory
+  B_Q_EMPTY = 1,     // the unit's last S has run
+  B_K_FULL = 2,      // +stage (3)
+  B_K_EMPTY = 5,     // +stage (3): the S of the stage's tile has run
+  B_V_FULL = 8,      // +stage (3)
+  B_V_EMPTY = 11,    // +stage (3): the P V of the stage's tile has run
+  B_S_FULL = 14,     // +buffer (3)
+  B_P_FULL = 17,     // count 4
+  B_O_DONE = 18,
+  B_O_FREE = 19,     // count 4
+  B_IDS_READY = 20,  // prefix pass: the chunk's block ids are staged
+  B_IDS_FREE = 21,   // prefix pass: the V producer is done with them
   N_BARS = 22
 };
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint32_t kTmemQ = 384;           // TMEM columns [384, 448): Q as bf16 pairs
+constexpr uint32_t kTmemO = 384;           // TMEM columns [384, 512): O (f32)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -234,12 +236,6 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned site) 
   atomicOr(&g_tc_err, site);
 }
 
-// Byte offset of 16-byte chunk c (0..15) of row r in a two-half, 128-row,
-// 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return (c >> 3) * kHalf + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -260,8 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t cnt = 1;
-      if (i == B_P_FULL || i == B_O_FREE || i == B_Q_EMPTY || i == B_QT_FULL) cnt = 4;
-      if (i >= B_KV_FULL && i < B_KV_FULL + kStages) cnt = 2;
+      if (i == B_P_FULL || i == B_O_FREE) cnt = 4;
       mbar_init(bar(i), cnt);
     }
     *abort = 0;
@@ -291,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_k = warp == 4;
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     const int stages = kStages;
-    const int b_full = B_KV_FULL;
-    const int b_empty = B_KV_EMPTY;
+    const int b_full = is_k ? B_K_FULL : B_V_FULL;
+    const int b_empty = is_k ? B_K_EMPTY : B_V_EMPTY;
     const uint32_t sm_base = sbase + (is_k ? SM_K : SM_V);
     if (lane == 0) {
       if (is_k) tma_prefetch_desc(&tm_q);
@@ -382,24 +377,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, 128, false, true);
-      const uint32_t t_o = tmem + 256;
+      const uint32_t t_o = tmem + kTmemO;
       uint32_t k_it = 0, v_it = 0, s_it = 0, p_it = 0, item_it = 0;
       bool failed = false;
+      const uint64_t d_q = sdesc_sw128(sbase + SM_Q, 16, 1024);
       auto issue_s = [&]() -> bool {
         const int st = k_it % kStages;
-        const int sb = s_it & 1;
-        // S buffer sb last held P of tile s_it - 2, read by a P V issued
+        const int sb = s_it % kSBufs;
+        // S buffer sb last held P of tile s_it - 3, read by a P V issued
         // before this MMA by this thread (tcgen05.mma runs in issue order)
-        // K and V of this tile (one wait for both; see mbar_try_wait_relaxed)
-        if (!mbar_wait_relaxed(bar(B_KV_FULL + st), (k_it / kStages) & 1, abort)) return false;
+        if (!mbar_wait_relaxed(bar(B_K_FULL + st), (k_it / kStages) & 1, abort)) return false;
         tc_fence_after();
-        const uint32_t ka = sbase + SM_K + st * 2 * kHalf;
+        const uint64_t d_k = sdesc_sw128(sbase + SM_K + st * 2 * kHalf, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          mma_bf16_ts(tmem + sb * 128, tmem + kTmemQ + kk * 8, sdesc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + sb * 128, d_q + off, d_k + off, id_qk, kk > 0);
         }
         mma_commit(bar(B_S_FULL + sb));
+        mma_commit(bar(B_K_EMPTY + st));
         ++k_it;
         ++s_it;
         return true;
@@ -408,22 +404,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit w = load_unit(p, u);
         const int n = count_tiles(p, w);
         if (n == 0) continue;
-        if (!mbar_wait_relaxed(bar(B_QT_FULL), item_it & 1, abort)) { failed = true; break; }
-        if (!issue_s()) { failed = true; break; }
+        if (!mbar_wait_relaxed(bar(B_Q_FULL), item_it & 1, abort)) { failed = true; break; }
+        // S runs two key tiles ahead of P V; Q is free once the unit's last S has run
+        int issued = 0;
+        auto issue_next = [&]() -> bool {
+          if (!issue_s()) return false;
+          if (++issued == n) mma_commit(bar(B_Q_EMPTY));
+          return true;
+        };
+        if (!issue_next()) { failed = true; break; }
+        if (n > 1 && !issue_next()) { failed = true; break; }
         for (int j = 0; j < n; ++j) {
-          if (j + 1 < n) {
-            if (!issue_s()) { failed = true; break; }
-          }
-          const int st = v_it % kStages;  // V landed with K, before S of this tile
+          if (issued < n && !issue_next()) { failed = true; break; }
+          const int st = v_it % kStages;
           if (j == 0 && !mbar_wait_relaxed(bar(B_O_FREE), (item_it & 1) ^ 1, abort)) { failed = true; break; }
+          if (!mbar_wait_relaxed(bar(B_V_FULL + st), (v_it / kStages) & 1, abort)) { failed = true; break; }
           if (!mbar_wait_relaxed(bar(B_P_FULL), p_it & 1, abort)) { failed = true; break; }
           tc_fence_after();
-          const uint32_t pt = tmem + (p_it & 1) * 128;  // P (bf16 pairs) over S of this tile
-          const uint32_t va = sbase + SM_V + st * 2 * kHalf;
+          const uint32_t pt = tmem + (p_it % kSBufs) * 128;  // P (bf16 pairs) over S of this tile
+          const uint64_t d_v = sdesc_sw128(sbase + SM_V + st * 2 * kHalf, kHalf, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(t_o, pt + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(B_KV_EMPTY + st));
+            mma_bf16_ts(t_o, pt + kk * 8, d_v + static_cast<uint64_t>(kk * (2048 >> 4)), id_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(B_V_EMPTY + st));
           mma_commit(bar(B_O_DONE));
           ++v_it;
           ++p_it;
@@ -436,36 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax (warps 0-3)
     const int r = threadIdx.x;  // query row == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t s_it = 0, p_it = 0, pv_base = 0, unit_it = 0;
+    uint32_t s_it = 0, p_it = 0, pv_base = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
       const Unit w = load_unit(p, u);
       const int n = count_tiles(p, w);
       if (n == 0) continue;
-      // Q row r into tensor memory as bf16 pairs (the A operand of S = Q K^T).
-      // Every S MMA of the previous unit has completed: this warp consumed
-      // all of their S tiles.
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL), unit_it & 1, abort))) { failed = true; break; }
-      {
-        uint32_t qk[64];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 v4 = *reinterpret_cast<const uint4*>(smem + SM_Q + sw128_off(r, c));
-          qk[4 * c + 0] = v4.x;
-          qk[4 * c + 1] = v4.y;
-          qk[4 * c + 2] = v4.z;
-          qk[4 * c + 3] = v4.w;
-        }
-        tmem_st64(tmem + lane_base + kTmemQ, qk);
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(B_QT_FULL));
-        mbar_arrive(bar(B_Q_EMPTY));
-      }
-      ++unit_it;
       // this thread's row
       bool valid;
       int32_t head, limit;  // limit: keys at positions >= limit are hidden (prefix) / causal bound (fwd)
@@ -493,8 +473,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileIter t;
       int j = 0;
       for (bool ok = tiles_begin(p, w, t); ok; ok = tiles_next(p, w, t), ++j) {
-        const int sb = s_it & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + sb), (s_it >> 1) & 1, abort))) { failed = true; break; }
+        const int sb = s_it % kSBufs;
+        // relaxed: only tensor-memory reads follow, ordered by the tcgen05 fence
+        if (!__all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_S_FULL + sb), (s_it / kSBufs) & 1, abort))) {
+          failed = true;
+          break;
+        }
         tc_fence_after();
         float s[128];
         {
@@ -580,18 +564,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // order (a parity wait is only sound one phase behind).  Once P V of
         // tile j-1 is done, O is stable and both P buffers are free.
         if (j > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (pv_base + j - 1) & 1, abort))) { failed = true; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_O_DONE), (pv_base + j - 1) & 1, abort))) {
+            failed = true;
+            break;
+          }
           tc_fence_after();
           if (__any_sync(0xffffffffu, grow)) {
             // O holds sums taken against the old max: rescale before P V of tile j
             uint32_t v[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              tmem_ld32(tmem + 256 + lane_base + c * 32, v);
+              tmem_ld32(tmem + kTmemO + lane_base + c * 32, v);
               tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(tmem + 256 + lane_base + c * 32, v);
+              tmem_st32(tmem + kTmemO + lane_base + c * 32, v);
             }
             tmem_wait_st();
           }
@@ -636,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t v[32];
-          tmem_ld32(tmem + 256 + lane_base + cc * 32, v);
+          tmem_ld32(tmem + kTmemO + lane_base + cc * 32, v);
           tmem_wait_ld();
           if (valid) {
             float acc[32];
@@ -677,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + 256 + lane_base + c * 32, v);
+        tmem_ld32(tmem + kTmemO + lane_base + c * 32, v);
         tmem_wait_ld();
         if (valid) {
           if (MODE == MODE_FWD) {
