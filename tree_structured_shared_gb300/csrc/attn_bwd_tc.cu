@@ -119,8 +119,9 @@ struct DqUnit {
 
 __device__ __forceinline__ DqUnit dq_unit(const DqParams& p, int u) {
   DqUnit w;
-  w.g = u % p.Hkv;
-  const FwdItem it = p.plan.items[u / p.Hkv];
+  // head-major: the CTAs at work at one time share one kv head's K/V
+  w.g = u / p.plan.n_items;
+  const FwdItem it = p.plan.items[u % p.plan.n_items];
   const QSeg qs = p.plan.qsegs[it.qseg];
   w.tile_start = it.tile_start;
   w.q_end = qs.q_start + qs.q_len;
@@ -489,8 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qd_it = 0, unit_it = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
-      const BwdItem it = p.plan.items[u / p.Hkv];
-      const int g = u % p.Hkv;
+      // head-major: the CTAs at work at one time share one kv head's Q / dO
+      const BwdItem it = p.plan.items[u % p.plan.n_items];
+      const int g = u / p.plan.n_items;
       QIter q;
       if (!q_begin(p, it, q)) continue;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_KV_EMPTY), (unit_it & 1) ^ 1, abort))) { failed = true; break; }
@@ -562,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(KB_SP_FULL));
       };
       for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
-        const BwdItem it = p.plan.items[u / p.Hkv];
+        const BwdItem it = p.plan.items[u % p.plan.n_items];
         QIter q;
         if (!q_begin(p, it, q)) continue;
         if (!mbar_wait_relaxed(bar(KB_KV_FULL), unit_it & 1, abort)) { failed = true; break; }
@@ -623,8 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qd_it = 0, g_it = 0, unit_it = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
-      const BwdItem it = p.plan.items[u / p.Hkv];
-      const int g = u % p.Hkv;
+      // head-major: the CTAs at work at one time share one kv head's Q / dO
+      const BwdItem it = p.plan.items[u % p.plan.n_items];
+      const int g = u / p.plan.n_items;
       QIter q;
       if (!q_begin(p, it, q)) continue;
       const int32_t key = it.k_start + r;

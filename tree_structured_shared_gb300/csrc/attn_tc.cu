@@ -65,7 +65,7 @@ constexpr int SM_V = SM_K + kStages * 2 * kHalf;
 constexpr int SM_P = SM_V + kStages * 2 * kHalf;
 constexpr int SM_BAR = SM_P;  // P lives in tensor memory, over the S tile it came from
 constexpr int SM_IDS = SM_BAR + 256;  // prefix pass: block ids of the unit's chunk
-constexpr int kMaxChunkBlocks = 384;
+constexpr int kMaxChunkBlocks = kMaxChunkTiles * kTileKeys / 16;
 constexpr int SM_TOTAL = SM_IDS + kMaxChunkBlocks * 4;
 constexpr int kSmemBytes = SM_TOTAL + 1024;
 
@@ -128,8 +128,12 @@ struct Unit {
 
 __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
   Unit w;
-  w.g = u % p.Hkv;
-  const int item = u / p.Hkv;
+  // forward: head-major, so the CTAs at work at one time share one kv head's
+  // K/V (a working set that stays in L2); decode: the heads of one item
+  // together
+  const int n_it = p.mode == MODE_FWD ? p.plan.n_items : 0;
+  w.g = p.mode == MODE_FWD ? u / n_it : u % p.Hkv;
+  const int item = p.mode == MODE_FWD ? u % n_it : u / p.Hkv;
   if (p.mode == MODE_FWD) {
     const FwdItem it = p.plan.items[item];
     const QSeg qs = p.plan.qsegs[it.qseg];
@@ -386,8 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sb = s_it % kSBufs;
         // S buffer sb last held P of tile s_it - 3, read by a P V issued
         // before this MMA by this thread (tcgen05.mma runs in issue order)
+        // TMA-written operands need no tcgen05 fence: the barrier's
+        // transaction count orders them before the MMA reads
         if (!mbar_wait_relaxed(bar(B_K_FULL + st), (k_it / kStages) & 1, abort)) return false;
-        tc_fence_after();
         const uint64_t d_k = sdesc_sw128(sbase + SM_K + st * 2 * kHalf, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {

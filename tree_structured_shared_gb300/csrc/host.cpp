@@ -1036,7 +1036,7 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
     work_tiles += static_cast<int64_t>(rt) * ((P[p] + kTileKeys - 1) / kTileKeys) * pool->Hkv;
   }
   int64_t ct = work_tiles / (2 * static_cast<int64_t>(n_sms));
-  ct = std::max<int64_t>(8, std::min<int64_t>(40, ct));
+  ct = std::max<int64_t>(8, std::min<int64_t>(kMaxChunkTiles, ct));
   int64_t rows = 0;
   for (int32_t p = 0; p < b->n_pages; ++p) {
     const int32_t b0 = b->branch_offsets[p], b1 = b->branch_offsets[p + 1];

@@ -25,6 +25,7 @@ struct FwdItem {
 
 constexpr int kTileKeys = 128;  // keys per K/V tile
 constexpr int kTileRows = 128;  // MMA M: query rows (tokens x heads of a GQA group)
+constexpr int kMaxChunkTiles = 40;  // prefix pass: key tiles in one chunk of a page's prefix, at most
 constexpr int kHeadDim = 128;   // d of the tensor-core path
 
 struct FwdPlan {
