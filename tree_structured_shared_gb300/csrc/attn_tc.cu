@@ -26,8 +26,8 @@
 //              chunk's block ids in shared memory.
 //   warp 6     producer of V tiles (TMA).
 //   warp 5     MMA issuer (one thread): S = Q K^T into one of three TMEM
-//              tiles, two key tiles ahead of the softmax, and O += P V (P read
-//              from TMEM) into a TMEM accumulator.
+//              tiles, two key tiles ahead of P V, and O += P V (P read from
+//              TMEM) into a TMEM accumulator.
 //
 // TMEM: columns [0,128), [128,256) and [256,384) hold S (then P), [384,512)
 // hold O (f32).  With three S tiles the S of tile j+2 needs only the P V of
@@ -74,17 +74,20 @@ enum {
   B_Q_FULL = 0,
   B_Q_EMPTY = 1,     // the unit's last S has run
   B_K_FULL = 2,      // +stage (3)
-  B_K_EMPTY = 5,     // +stage (3): the S of the stage's tile has run
-  B_V_FULL = 8,      // +stage (3)
-  B_V_EMPTY = 11,    // +stage (3): the P V of the stage's tile has run
-  B_S_FULL = 14,     // +buffer (3)
-  B_P_FULL = 17,     // count 4
-  B_O_DONE = 18,
-  B_O_FREE = 19,     // count 4
-  B_IDS_READY = 20,  // prefix pass: the chunk's block ids are staged
-  B_IDS_FREE = 21,   // prefix pass: the V producer is done with them
-  N_BARS = 22
+  B_V_FULL = 5,      // +stage (3)
+  B_S_FULL = 8,      // +buffer (3): S of tile k (buffer and K stage k % 3) has run
+  B_P_FULL = 11,     // +buffer (3), count 4: P of the tile in that S buffer is written
+  B_O_DONE = 14,     // +buffer (3): P V of tile k (V stage k % 3) has run
+  B_O_FREE = 17,     // count 4
+  B_IDS_READY = 18,  // prefix pass: the chunk's block ids are staged
+  B_IDS_FREE = 19,   // prefix pass: the V producer is done with them
+  N_BARS = 20
 };
+// Key tile k uses K stage, S buffer and V stage k % 3 alike, so the S_FULL
+// commit also frees its K stage and the O_DONE commit its V stage: the
+// producers wait on those, and the MMA thread issues two commits per tile.
+static_assert(kStages == kSBufs, "K / V stages must match the S buffers");
+static_assert(N_BARS * 8 + 8 <= SM_IDS - SM_BAR, "barrier area");
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kTmemO = 384;           // TMEM columns [384, 512): O (f32)
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t cnt = 1;
-      if (i == B_P_FULL || i == B_O_FREE) cnt = 4;
+      if ((i >= B_P_FULL && i < B_P_FULL + kSBufs) || i == B_O_FREE) cnt = 4;
       mbar_init(bar(i), cnt);
     }
     *abort = 0;
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     const int stages = kStages;
     const int b_full = is_k ? B_K_FULL : B_V_FULL;
-    const int b_empty = is_k ? B_K_EMPTY : B_V_EMPTY;
+    const int b_empty = is_k ? B_S_FULL : B_O_DONE;  // the S / P V of the stage's last tile has run
     const uint32_t sm_base = sbase + (is_k ? SM_K : SM_V);
     if (lane == 0) {
       if (is_k) tma_prefetch_desc(&tm_q);
@@ -378,31 +381,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (failed && lane == 0) raise_abort(abort, is_k ? 0x1 : 0x2);
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    // tcgen05.mma issue stalls while the pipe is full, so every instruction
+    // between two MMA groups is pipe idle time: ring positions are kept as
+    // (index, phase) pairs, and each tile costs two commits and three waits.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, 128, false, true);
       const uint32_t t_o = tmem + kTmemO;
-      uint32_t k_it = 0, v_it = 0, s_it = 0, p_it = 0, item_it = 0;
-      bool failed = false;
       const uint64_t d_q = sdesc_sw128(sbase + SM_Q, 16, 1024);
+      uint32_t sb = 0, s_ph = 0;  // ring position of the next S (K stage = S buffer)
+      uint32_t pb = 0, p_ph = 0;  // ring position of the next P V (V stage = S buffer)
+      uint32_t item_it = 0;
+      bool failed = false;
+      // S of the next key tile.  Its S buffer last held P of the tile three
+      // back, read by a P V issued earlier by this thread (tcgen05.mma runs
+      // in issue order).  TMA-written operands need no tcgen05 fence: the
+      // barrier's transaction count orders them before the MMA reads.
       auto issue_s = [&]() -> bool {
-        const int st = k_it % kStages;
-        const int sb = s_it % kSBufs;
-        // S buffer sb last held P of tile s_it - 3, read by a P V issued
-        // before this MMA by this thread (tcgen05.mma runs in issue order)
-        // TMA-written operands need no tcgen05 fence: the barrier's
-        // transaction count orders them before the MMA reads
-        if (!mbar_wait_relaxed(bar(B_K_FULL + st), (k_it / kStages) & 1, abort)) return false;
-        const uint64_t d_k = sdesc_sw128(sbase + SM_K + st * 2 * kHalf, 16, 1024);
+        if (!mbar_wait_relaxed(bar(B_K_FULL + sb), s_ph, abort)) return false;
+        const uint64_t d_k = sdesc_sw128(sbase + SM_K + sb * 2 * kHalf, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
           mma_bf16_ss(tmem + sb * 128, d_q + off, d_k + off, id_qk, kk > 0);
         }
         mma_commit(bar(B_S_FULL + sb));
-        mma_commit(bar(B_K_EMPTY + st));
-        ++k_it;
-        ++s_it;
+        if (++sb == kSBufs) {
+          sb = 0;
+          s_ph ^= 1;
+        }
         return true;
       };
       for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
@@ -411,31 +418,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n == 0) continue;
         if (!mbar_wait_relaxed(bar(B_Q_FULL), item_it & 1, abort)) { failed = true; break; }
         // S runs two key tiles ahead of P V; Q is free once the unit's last S has run
-        int issued = 0;
-        auto issue_next = [&]() -> bool {
-          if (!issue_s()) return false;
-          if (++issued == n) mma_commit(bar(B_Q_EMPTY));
-          return true;
-        };
-        if (!issue_next()) { failed = true; break; }
-        if (n > 1 && !issue_next()) { failed = true; break; }
+        if (!issue_s()) { failed = true; break; }
+        if (n > 1 && !issue_s()) { failed = true; break; }
+        if (n <= 2) mma_commit(bar(B_Q_EMPTY));
         for (int j = 0; j < n; ++j) {
-          if (issued < n && !issue_next()) { failed = true; break; }
-          const int st = v_it % kStages;
+          if (j + 2 < n) {
+            if (!issue_s()) { failed = true; break; }
+            if (j + 3 == n) mma_commit(bar(B_Q_EMPTY));
+          }
           if (j == 0 && !mbar_wait_relaxed(bar(B_O_FREE), (item_it & 1) ^ 1, abort)) { failed = true; break; }
-          if (!mbar_wait_relaxed(bar(B_V_FULL + st), (v_it / kStages) & 1, abort)) { failed = true; break; }
-          if (!mbar_wait_relaxed(bar(B_P_FULL), p_it & 1, abort)) { failed = true; break; }
+          if (!mbar_wait_relaxed(bar(B_V_FULL + pb), p_ph, abort)) { failed = true; break; }
+          // per-buffer barriers: the softmax may run up to two tiles ahead
+          if (!mbar_wait_relaxed(bar(B_P_FULL + pb), p_ph, abort)) { failed = true; break; }
           tc_fence_after();
-          const uint32_t pt = tmem + (p_it % kSBufs) * 128;  // P (bf16 pairs) over S of this tile
-          const uint64_t d_v = sdesc_sw128(sbase + SM_V + st * 2 * kHalf, kHalf, 1024);
+          const uint32_t pt = tmem + pb * 128;  // P (bf16 pairs) over S of this tile
+          const uint64_t d_v = sdesc_sw128(sbase + SM_V + pb * 2 * kHalf, kHalf, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(t_o, pt + kk * 8, d_v + static_cast<uint64_t>(kk * (2048 >> 4)), id_pv,
                         (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(B_V_EMPTY + st));
-          mma_commit(bar(B_O_DONE));
-          ++v_it;
-          ++p_it;
+          mma_commit(bar(B_O_DONE + pb));
+          if (++pb == kSBufs) {
+            pb = 0;
+            p_ph ^= 1;
+          }
         }
         ++item_it;
       }
@@ -565,16 +571,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) f2unpack(l2[k], l8[2 * k], l8[2 * k + 1]);
           l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         }
-        // Every P V product completes one O_DONE phase; wait for each one in
-        // order (a parity wait is only sound one phase behind).  Once P V of
-        // tile j-1 is done, O is stable and both P buffers are free.
-        if (j > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_O_DONE), (pv_base + j - 1) & 1, abort))) {
+        // Only a rescale of O waits for P V of tile j-1.  P V number q
+        // completes a phase of O_DONE + q % 3 (phase q / 3); the barrier
+        // cannot run a phase ahead of this wait, because P V q + 3 needs a P
+        // this warp has not written yet.  Writing P needs no wait: its S
+        // buffer last held P of tile j-3, whose P V ran before S of tile j.
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          const uint32_t q = pv_base + j - 1;
+          if (!__all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_O_DONE + q % kSBufs), (q / kSBufs) & 1, abort))) {
             failed = true;
             break;
           }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, grow)) {
+          {
             // O holds sums taken against the old max: rescale before P V of tile j
             uint32_t v[32];
 #pragma unroll
@@ -598,12 +607,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_P_FULL));
+        if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
         ++p_it;
       }
       if (failed) break;
       // epilogue: O / l and LSE
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (pv_base + n - 1) & 1, abort))) { failed = true; break; }
+      {
+        // the unit's last P V (its commit covers all earlier ones)
+        const uint32_t q = pv_base + n - 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE + q % kSBufs), (q / kSBufs) & 1, abort))) {
+          failed = true;
+          break;
+        }
+      }
       tc_fence_after();
       if (MODE == MODE_OWN) {
         // merge with the prefix pass's partial rows of this (query, head) by
