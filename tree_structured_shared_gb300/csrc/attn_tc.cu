@@ -24,7 +24,8 @@
 //              the max grows by more than 2^8, and runs the epilogue.
 //   warp 4     producer of Q and K tiles (TMA); decode: also stages the
 //              chunk's block ids in shared memory.
-//   warp 6     producer of V tiles (TMA).
+//   warp 6     producer of V tiles (TMA); a V tile's bytes complete the
+//              P_FULL barrier of its key tile, next to the softmax's P.
 //   warp 5     MMA issuer (one thread): S = Q K^T into one of three TMEM
 //              tiles, two key tiles ahead of P V, and O += P V (P read from
 //              TMEM) into a TMEM accumulator.
@@ -34,7 +35,8 @@
 // tile j-1 to have been issued, so the softmax never waits for its next S.
 // K and V have rings of their own: a K stage is free once its S has run, a V
 // stage once its P V has, so each ring prefetches as far as its lifetime
-// allows.
+// allows.  tcgen05.mma issue stalls while the pipe is full, so the MMA
+// thread does little else: two waits and two commits per key tile.
 // Shared memory (1024-byte aligned, 128-byte swizzle, two 64-column halves):
 //   Q 32 KB | K 3 x 32 KB | V 3 x 32 KB | barriers | block ids.
 // Every wait is bounded; a unit that times out raises the CTA abort flag, the
@@ -74,18 +76,18 @@ enum {
   B_Q_FULL = 0,
   B_Q_EMPTY = 1,     // the unit's last S has run
   B_K_FULL = 2,      // +stage (3)
-  B_V_FULL = 5,      // +stage (3)
-  B_S_FULL = 8,      // +buffer (3): S of tile k (buffer and K stage k % 3) has run
-  B_P_FULL = 11,     // +buffer (3), count 4: P of the tile in that S buffer is written
-  B_O_DONE = 14,     // +buffer (3): P V of tile k (V stage k % 3) has run
-  B_O_FREE = 17,     // count 4
-  B_IDS_READY = 18,  // prefix pass: the chunk's block ids are staged
-  B_IDS_FREE = 19,   // prefix pass: the V producer is done with them
-  N_BARS = 20
+  B_S_FULL = 5,      // +buffer (3): S of tile k (buffer and K stage k % 3) has run
+  B_P_FULL = 8,      // +buffer (3), count 5: P of tile k is written and its V has landed
+  B_O_DONE = 11,     // +buffer (3): P V of tile k (V stage k % 3) has run
+  B_IDS_READY = 14,  // prefix pass: the chunk's block ids are staged
+  B_IDS_FREE = 15,   // prefix pass: the V producer is done with them
+  N_BARS = 16
 };
 // Key tile k uses K stage, S buffer and V stage k % 3 alike, so the S_FULL
 // commit also frees its K stage and the O_DONE commit its V stage: the
-// producers wait on those, and the MMA thread issues two commits per tile.
+// producers wait on those.  The V tile's bytes land on P_FULL (one arrival of
+// the V producer plus the four softmax warps), so P V waits once.  The MMA
+// thread thus issues two commits and two waits per tile.
 static_assert(kStages == kSBufs, "K / V stages must match the S buffers");
 static_assert(N_BARS * 8 + 8 <= SM_IDS - SM_BAR, "barrier area");
 
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t cnt = 1;
-      if ((i >= B_P_FULL && i < B_P_FULL + kSBufs) || i == B_O_FREE) cnt = 4;
+      if (i >= B_P_FULL && i < B_P_FULL + kSBufs) cnt = 5;
       mbar_init(bar(i), cnt);
     }
     *abort = 0;
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_k = warp == 4;
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     const int stages = kStages;
-    const int b_full = is_k ? B_K_FULL : B_V_FULL;
+    const int b_full = is_k ? B_K_FULL : B_P_FULL;
     const int b_empty = is_k ? B_S_FULL : B_O_DONE;  // the S / P V of the stage's last tile has run
     const uint32_t sm_base = sbase + (is_k ? SM_K : SM_V);
     if (lane == 0) {
@@ -426,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!issue_s()) { failed = true; break; }
             if (j + 3 == n) mma_commit(bar(B_Q_EMPTY));
           }
-          if (j == 0 && !mbar_wait_relaxed(bar(B_O_FREE), (item_it & 1) ^ 1, abort)) { failed = true; break; }
-          if (!mbar_wait_relaxed(bar(B_V_FULL + pb), p_ph, abort)) { failed = true; break; }
-          // per-buffer barriers: the softmax may run up to two tiles ahead
+          // P and V of this tile (per-buffer barriers: the softmax may run up
+          // to two tiles ahead).  The first P of a unit is written after the
+          // softmax's epilogue read O, so P V may then overwrite O.
           if (!mbar_wait_relaxed(bar(B_P_FULL + pb), p_ph, abort)) { failed = true; break; }
           tc_fence_after();
           const uint32_t pt = tmem + pb * 128;  // P (bf16 pairs) over S of this tile
@@ -673,9 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   pack_bf16x2(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_O_FREE));
+        // O is read: this warp's next P_FULL arrival (after its own
+        // tcgen05.fence::before_thread_sync) lets P V overwrite it
         if (valid) p.lse[qpos * p.Hq + head] = L > 0.f ? (Mu + __log2f(L)) * kLn2 : -INFINITY;
         pv_base += n;
         continue;
@@ -706,9 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_O_FREE));
+      // O is read: this warp's next P_FULL arrival (after its own
+      // tcgen05.fence::before_thread_sync) lets P V overwrite it
       if (valid) {
         if (MODE == MODE_FWD)
           p.lse[static_cast<int64_t>(head) * p.T + qpos] = lse_v;
