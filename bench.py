@@ -226,6 +226,13 @@ def traffic_for(kernel: str, units: float):
     return d["dram_bytes"] / d["units"] * units
 
 
+def bwd_traffic(units: float):
+    """DRAM bytes of the dQ and dK/dV passes (the row-sum pass is not
+    captured), or None when either kernel changed since the capture."""
+    a, b = traffic_for("bwd_dq", units), traffic_for("bwd_dkv", units)
+    return None if a is None or b is None else a + b
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,7 +429,8 @@ def main() -> int:
                      "tflops_per_gpu": bwd.flops / (t_bwd * 1e-3) / 1e12, "bound": "tensor", "peak": tf_sus,
                      "peak_kind": "bf16 sustained " + peak_src,
                      "frac": bwd.flops / (t_bwd * 1e-3) / 1e12 / tf_sus, "algorithmic_flops": bwd.flops,
-                     "what": "dQ, dK, dV of the same forward (launches: row sums, dQ pass, dK/dV pass)"},
+                     "what": "dQ, dK, dV of the same forward (launches: row sums, dQ pass, dK/dV pass)",
+                     "traffic": bwd_traffic(fw.n_tokens)},
         "gpu_launches": ((5 if acc is not None else 3) + 3) * K,
         "clocks": clk,
     }
