@@ -73,21 +73,24 @@ constexpr int kSmemBytes = SM_TOTAL + 1024;
 
 // barrier slots
 enum {
-  B_Q_FULL = 0,
+  B_QK0_FULL = 0,    // count 2: Q and the K tile of the unit's first key tile have landed
   B_Q_EMPTY = 1,     // the unit's last S has run
-  B_K_FULL = 2,      // +stage (3)
-  B_S_FULL = 5,      // +buffer (3): S of tile k (buffer and K stage k % 3) has run
-  B_P_FULL = 8,      // +buffer (3), count 5: P of tile k is written and its V has landed
-  B_O_DONE = 11,     // +buffer (3): P V of tile k (V stage k % 3) has run
-  B_IDS_READY = 14,  // prefix pass: the chunk's block ids are staged
-  B_IDS_FREE = 15,   // prefix pass: the V producer is done with them
-  N_BARS = 16
+  B_K1_FULL = 2,     // the K tile of the unit's second key tile has landed
+  B_S_FULL = 3,      // +buffer (3): S of tile k (buffer and K stage k % 3) has run
+  B_P_FULL = 6,      // +buffer (3), count 6: see below
+  B_O_DONE = 9,      // +buffer (3): P V of tile k (V stage k % 3) has run
+  B_IDS_READY = 12,  // prefix pass: the chunk's block ids are staged
+  B_IDS_FREE = 13,   // prefix pass: the V producer is done with them
+  N_BARS = 14
 };
-// Key tile k uses K stage, S buffer and V stage k % 3 alike, so the S_FULL
-// commit also frees its K stage and the O_DONE commit its V stage: the
-// producers wait on those.  The V tile's bytes land on P_FULL (one arrival of
-// the V producer plus the four softmax warps), so P V waits once.  The MMA
-// thread thus issues two commits and two waits per tile.
+// Tiles are numbered k across all units of the CTA.  Tile k uses K stage, S
+// buffer and V stage k % 3 alike, so the S_FULL commit also frees its K stage
+// and the O_DONE commit its V stage: the producers wait on those.  P_FULL of
+// tile k completes with six arrivals: the four softmax warps (P written), the
+// V producer (V of tile k landed) and the K producer (K of the unit's tile
+// two further on landed, or a plain arrival near the unit's end).  So the MMA
+// thread waits once per key tile, issues S of tile k+2 and P V of tile k, and
+// commits twice.
 static_assert(kStages == kSBufs, "K / V stages must match the S buffers");
 static_assert(N_BARS * 8 + 8 <= SM_IDS - SM_BAR, "barrier area");
 
@@ -265,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t cnt = 1;
-      if (i >= B_P_FULL && i < B_P_FULL + kSBufs) cnt = 5;
+      if (i >= B_P_FULL && i < B_P_FULL + kSBufs) cnt = 6;
+      if (i == B_QK0_FULL) cnt = 2;
       mbar_init(bar(i), cnt);
     }
     *abort = 0;
@@ -295,7 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_k = warp == 4;
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     const int stages = kStages;
-    const int b_full = is_k ? B_K_FULL : B_P_FULL;
     const int b_empty = is_k ? B_S_FULL : B_O_DONE;  // the S / P V of the stage's last tile has run
     const uint32_t sm_base = sbase + (is_k ? SM_K : SM_V);
     if (lane == 0) {
@@ -311,19 +314,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (item_it & 1) ^ 1, abort))) { failed = true; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * kHalf);
+          mbar_arrive_expect_tx(bar(B_QK0_FULL), 2 * kHalf);
           if (MODE == MODE_FWD) {
             const int tt = p.plan.tile_tokens;
             for (int hh = 0; hh < G; ++hh)
               for (int h = 0; h < 2; ++h)
-                tma_load_3d(sbase + SM_Q + h * kHalf + hh * tt * 128, &tm_q, bar(B_Q_FULL), h * 64, w.g * G + hh,
+                tma_load_3d(sbase + SM_Q + h * kHalf + hh * tt * 128, &tm_q, bar(B_QK0_FULL), h * 64, w.g * G + hh,
                             w.tile_start);
           } else {
             // Query rows of the page, row R = (query R / G, head g*G + R % G):
             // a 4-D box {d/2, G, 1, 128/G} of q viewed as [nq][Hkv][G][d]
             // lands in exactly that row order.
             const int q0 = MODE == MODE_OWN ? w.q_first : w.q_first + w.tile * (kTileRows / G);
-            for (int h = 0; h < 2; ++h) tma_load_4d(sbase + SM_Q + h * kHalf, &tm_q, bar(B_Q_FULL), h * 64, 0, w.g, q0);
+            for (int h = 0; h < 2; ++h) tma_load_4d(sbase + SM_Q + h * kHalf, &tm_q, bar(B_QK0_FULL), h * 64, 0, w.g, q0);
           }
         }
         if (MODE == MODE_PREFIX) {
@@ -338,23 +341,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (MODE == MODE_PREFIX) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_IDS_READY), item_it & 1, abort))) { failed = true; break; }
       }
+      const uint32_t it0 = it;  // number of the unit's first tile
       TileIter t;
       for (bool ok = tiles_begin(p, w, t); ok; ok = tiles_next(p, w, t), ++it) {
         const int st = it % stages;
         const uint32_t ph = ((it / stages) & 1) ^ 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(b_empty + st), ph, abort))) { failed = true; break; }
         const uint32_t dst = sm_base + st * 2 * kHalf;
+        // where the tile's bytes land: V on P_FULL of its own tile; K of the
+        // unit's first two tiles on QK0 / K1, later K on P_FULL of the tile
+        // two before it (S of that K tile is issued after that wait)
+        const int b_full = !is_k ? B_P_FULL + st
+                                 : (it == it0 ? B_QK0_FULL
+                                              : (it == it0 + 1 ? B_K1_FULL : B_P_FULL + (it - 2) % kSBufs));
         if (MODE == MODE_FWD) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(bar(b_full + st), 2 * kHalf);
-            for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kHalf, tm, bar(b_full + st), h * 64, w.g, t.ks);
+            mbar_arrive_expect_tx(bar(b_full), 2 * kHalf);
+            for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kHalf, tm, bar(b_full), h * 64, w.g, t.ks);
           }
         } else if (MODE == MODE_OWN && t.s == 1) {
           // the query block's own keys: 16 rows of k_new / v_new for kv head g
           if (lane == 0) {
-            mbar_arrive_expect_tx(bar(b_full + st), 2 * 2048);
+            mbar_arrive_expect_tx(bar(b_full), 2 * 2048);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(dst + h * kHalf, is_k ? &tm_kn : &tm_vn, bar(b_full + st), h * 64, w.g, w.q_first);
+              tma_load_3d(dst + h * kHalf, is_k ? &tm_kn : &tm_vn, bar(b_full), h * 64, w.g, w.q_first);
           }
         } else {
           const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
@@ -365,15 +375,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (lane < nblk) {
             blk = ids[((t.ks - w.k_begin) >> 4) + lane];
           }
-          if (lane == 0) mbar_arrive_expect_tx(bar(b_full + st), nblk * 2 * 2048);
+          if (lane == 0) mbar_arrive_expect_tx(bar(b_full), nblk * 2 * 2048);
           __syncwarp();
           if (lane < nblk) {
             const int32_t row = (blk * p.Hkv + w.g) * 16;
-            for (int h = 0; h < 2; ++h) tma_load_2d(dst + h * kHalf + lane * 2048, tm, bar(b_full + st), h * 64, row);
+            for (int h = 0; h < 2; ++h) tma_load_2d(dst + h * kHalf + lane * 2048, tm, bar(b_full), h * 64, row);
           }
         }
       }
       if (failed) break;
+      if (is_k) {
+        // tiles whose K tile two further on does not exist (the unit's last
+        // two) still get the K producer's arrival on P_FULL.  Arriving for
+        // tile k needs P_FULL of tile k-3 complete: S of tile k-1 is issued
+        // only after that, so wait for S of tile k-1.
+        const uint32_t n_t = it - it0;
+        for (uint32_t k = it0 + (n_t > 2 ? n_t - 2 : 0); k < it && !failed; ++k) {
+          if (k > 0 &&
+              !__all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + (k - 1) % kSBufs), ((k - 1) / kSBufs) & 1, abort)))
+            failed = true;
+          if (!failed && lane == 0) mbar_arrive(bar(B_P_FULL + k % kSBufs));
+        }
+        if (failed) break;
+      }
       if (!is_k && MODE == MODE_PREFIX) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_IDS_FREE));
@@ -385,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // tcgen05.mma issue stalls while the pipe is full, so every instruction
     // between two MMA groups is pipe idle time: ring positions are kept as
-    // (index, phase) pairs, and each tile costs two commits and three waits.
+    // (index, phase) pairs, and each key tile costs one wait and two commits.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, 128, false, true);
@@ -393,14 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t d_q = sdesc_sw128(sbase + SM_Q, 16, 1024);
       uint32_t sb = 0, s_ph = 0;  // ring position of the next S (K stage = S buffer)
       uint32_t pb = 0, p_ph = 0;  // ring position of the next P V (V stage = S buffer)
-      uint32_t item_it = 0;
+      uint32_t item_it = 0, k1_it = 0;
       bool failed = false;
-      // S of the next key tile.  Its S buffer last held P of the tile three
-      // back, read by a P V issued earlier by this thread (tcgen05.mma runs
-      // in issue order).  TMA-written operands need no tcgen05 fence: the
-      // barrier's transaction count orders them before the MMA reads.
-      auto issue_s = [&]() -> bool {
-        if (!mbar_wait_relaxed(bar(B_K_FULL + sb), s_ph, abort)) return false;
+      // S of the next key tile, its K tile already waited for.  Its S buffer
+      // last held P of the tile three back, read by a P V issued earlier by
+      // this thread (tcgen05.mma runs in issue order).  TMA-written operands
+      // need no tcgen05 fence: the barrier's transaction count orders them
+      // before the MMA reads.
+      auto issue_s = [&]() {
         const uint64_t d_k = sdesc_sw128(sbase + SM_K + sb * 2 * kHalf, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -412,27 +436,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           sb = 0;
           s_ph ^= 1;
         }
-        return true;
       };
       for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
         const Unit w = load_unit(p, u);
         const int n = count_tiles(p, w);
         if (n == 0) continue;
-        if (!mbar_wait_relaxed(bar(B_Q_FULL), item_it & 1, abort)) { failed = true; break; }
         // S runs two key tiles ahead of P V; Q is free once the unit's last S has run
-        if (!issue_s()) { failed = true; break; }
-        if (n > 1 && !issue_s()) { failed = true; break; }
+        if (!mbar_wait_relaxed(bar(B_QK0_FULL), item_it & 1, abort)) { failed = true; break; }
+        issue_s();
+        if (n > 1) {
+          if (!mbar_wait_relaxed(bar(B_K1_FULL), k1_it & 1, abort)) { failed = true; break; }
+          ++k1_it;
+          issue_s();
+        }
         if (n <= 2) mma_commit(bar(B_Q_EMPTY));
         for (int j = 0; j < n; ++j) {
-          if (j + 2 < n) {
-            if (!issue_s()) { failed = true; break; }
-            if (j + 3 == n) mma_commit(bar(B_Q_EMPTY));
-          }
-          // P and V of this tile (per-buffer barriers: the softmax may run up
-          // to two tiles ahead).  The first P of a unit is written after the
-          // softmax's epilogue read O, so P V may then overwrite O.
+          // P and V of tile j and K of tile j+2 land on one per-buffer
+          // barrier (the softmax may run up to two tiles ahead).  The first P
+          // of a unit is written after the softmax's epilogue read O, so P V
+          // may then overwrite O.
           if (!mbar_wait_relaxed(bar(B_P_FULL + pb), p_ph, abort)) { failed = true; break; }
           tc_fence_after();
+          if (j + 2 < n) {
+            issue_s();
+            if (j + 3 == n) mma_commit(bar(B_Q_EMPTY));
+          }
           const uint32_t pt = tmem + pb * 128;  // P (bf16 pairs) over S of this tile
           const uint64_t d_v = sdesc_sw128(sbase + SM_V + pb * 2 * kHalf, kHalf, 1024);
 #pragma unroll
