@@ -23,7 +23,9 @@
 //              pairs) back over the S tile in TMEM, rescales O in TMEM when
 //              the max grows by more than 2^8, and runs the epilogue.
 //   warp 4     producer of Q and K tiles (TMA); decode: also stages the
-//              chunk's block ids in shared memory.
+//              chunk's block ids in shared memory.  Q and a unit's first K
+//              tile share a barrier, the second K tile has its own, and later
+//              K tiles complete the P_FULL barrier of the tile two before.
 //   warp 6     producer of V tiles (TMA); a V tile's bytes complete the
 //              P_FULL barrier of its key tile, next to the softmax's P.
 //   warp 5     MMA issuer (one thread): S = Q K^T into one of three TMEM
@@ -36,7 +38,7 @@
 // K and V have rings of their own: a K stage is free once its S has run, a V
 // stage once its P V has, so each ring prefetches as far as its lifetime
 // allows.  tcgen05.mma issue stalls while the pipe is full, so the MMA
-// thread does little else: two waits and two commits per key tile.
+// thread does little else: one wait and two commits per key tile.
 // Shared memory (1024-byte aligned, 128-byte swizzle, two 64-column halves):
 //   Q 32 KB | K 3 x 32 KB | V 3 x 32 KB | barriers | block ids.
 // Every wait is bounded; a unit that times out raises the CTA abort flag, the
