@@ -383,6 +383,11 @@ def main() -> int:
     hbm = float(peaks["hbm_gbs"])
     tf_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     own_b, pre_b, all_b = dec.own_bytes(), dec.prefix_bytes(), dec.unique_kv_bytes()
+    # algorithmic flops (4 d Hq per query-ancestor pair): the whole step, and
+    # the prefix pass's share (each query row against its page prefix)
+    dec_fl = dec.flops()
+    pre_fl = 4.0 * dw.d * dw.Hq * sum(pg.q_len[j] * pg.branch_prefix_len[j] for pg in dw.pages
+                                      for j in range(len(pg.q_len)))
     fl = fwd.flops
     own_gbs = own_b / (t_own * 1e-3) / 1e9
     pre_gbs = pre_b / (t_pre * 1e-3) / 1e9
@@ -414,12 +419,17 @@ def main() -> int:
                      "traffic": traffic_for("own_pass", own_units), "algorithmic_bytes": own_b, "ms": t_own},
         "kernels": {
             "prefix_pass": {"ms": t_pre, "achieved_gbs": pre_gbs, "frac_hbm": pre_gbs / hbm,
-                            "algorithmic_bytes": pre_b,
+                            "algorithmic_bytes": pre_b, "algorithmic_flops": pre_fl,
+                            "achieved_tflops": pre_fl / (t_pre * 1e-3) / 1e12,
+                            "frac_tensor": pre_fl / (t_pre * 1e-3) / 1e12 / tf_sus,
+                            "bound_time_ms": max(pre_b / (hbm * 1e9), pre_fl / (tf_sus * 1e12)) * 1e3,
                             "traffic": traffic_for("prefix_pass", sum(max(p.branch_prefix_len or [0]) for p in dw.pages))},
             "own_pass": {"ms": t_own, "achieved_gbs": own_gbs, "frac_hbm": own_gbs / hbm,
                          "algorithmic_bytes": own_b},
             "decode_step": {"ms": t_dec, "achieved_gbs": dec_gbs, "frac_hbm": dec_gbs / hbm,
-                            "frac_spec_8tbs": dec_gbs / 8000.0, "algorithmic_bytes": all_b},
+                            "frac_spec_8tbs": dec_gbs / 8000.0, "algorithmic_bytes": all_b,
+                            "algorithmic_flops": dec_fl, "frac_tensor": dec_fl / (t_dec * 1e-3) / 1e12 / tf_sus,
+                            "bound_time_ms": max(all_b / (hbm * 1e9), dec_fl / (tf_sus * 1e12)) * 1e3},
         },
         "forward": {"ms": t_fwd, "tflops": fwd_tf * world, "tflops_per_gpu": fwd_tf, "bound": "tensor",
                     "peak": tf_sus, "peak_kind": "bf16 sustained " + peak_src, "frac": fwd_tf / tf_sus,
