@@ -389,6 +389,7 @@ def main() -> int:
     pre_fl = 4.0 * dw.d * dw.Hq * sum(pg.q_len[j] * pg.branch_prefix_len[j] for pg in dw.pages
                                       for j in range(len(pg.q_len)))
     fl = fwd.flops
+    fwd_ex = fwd.executed_flops  # tensor-core work incl. masked / padded tile elements
     own_gbs = own_b / (t_own * 1e-3) / 1e9
     pre_gbs = pre_b / (t_pre * 1e-3) / 1e9
     dec_gbs = all_b / (t_dec * 1e-3) / 1e9
@@ -434,6 +435,7 @@ def main() -> int:
         "forward": {"ms": t_fwd, "tflops": fwd_tf * world, "tflops_per_gpu": fwd_tf, "bound": "tensor",
                     "peak": tf_sus, "peak_kind": "bf16 sustained " + peak_src, "frac": fwd_tf / tf_sus,
                     "frac_spec_2250": fwd_tf / 2250.0, "algorithmic_flops": fl,
+                    "executed_flops": fwd_ex, "executed_frac": fwd_ex / (t_fwd * 1e-3) / 1e12 / tf_sus,
                     "traffic": traffic_for("forward", fw.n_tokens)},
         "backward": {"ms": t_bwd, "tflops": bwd.flops / (t_bwd * 1e-3) / 1e12 * world,
                      "tflops_per_gpu": bwd.flops / (t_bwd * 1e-3) / 1e12, "bound": "tensor", "peak": tf_sus,

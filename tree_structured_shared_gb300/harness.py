@@ -60,6 +60,26 @@ class Forward:
         """Algorithmic flops: 4 d Hq per (query, ancestor) pair."""
         return 4.0 * self.w.d * self.w.Hq * self.desc.info()["ancestor_pairs"]
 
+    @property
+    def executed_flops(self) -> float:
+        """Flops the tensor cores execute on the bf16 path: per (query tile,
+        kv head) unit, S and P V over every 128-key tile the unit walks (the
+        key tiles of each of its key segments, a causal one cut at the tile's
+        last token), 128 x 128 x d x 2 x 2 each -- masked and padded elements
+        included."""
+        w = self.w
+        tt = 128 // (w.Hq // w.Hkv)
+        qs, kv = self.desc.segments()
+        tiles = 0
+        for q_start, q_len, kv_first, kv_count in qs.tolist():
+            for t0 in range(q_start, q_start + q_len, tt):
+                last = min(t0 + tt, q_start + q_len) - 1
+                for ks, kl, causal in kv[kv_first:kv_first + kv_count].tolist():
+                    end = min(ks + kl, last + 1) if causal else ks + kl
+                    if end > ks:
+                        tiles += (end - ks + 127) // 128
+        return float(tiles) * w.Hkv * 128 * 128 * w.d * 2 * 2
+
 
 class Backward:
     """The backward of a Forward: upstream gradient dO resident on the GPU,
