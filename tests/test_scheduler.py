@@ -155,3 +155,43 @@ def test_rejects_bad_arguments(padoc_lib):
         cs.update(0, [(0, [5])])  # not running
     with pytest.raises(padoc.PadocError):
         cs.output(0)
+
+
+class PortSched:
+    """The C++ scheduler behind the golden replay's interface: batches come
+    back as (page request, branch ids), the page's pool sequence checked."""
+
+    def __init__(self, blocks, tau, n_max, window, max_len):
+        self.pool = padoc.KVPool(FAKE, FAKE, blocks, Hkv=2, d=128, max_seqs=64, max_blocks_per_seq=64)
+        self.s = padoc.Scheduler(self.pool, tau, n_max, window, max_len, FORK, CHILD, EOS)
+
+    def submit(self, prompt, at):
+        return self.s.submit(prompt, at)
+
+    def schedule(self, step):
+        adm, pre, pages = self.s.schedule()
+        out = []
+        for pseq, br in pages:
+            rids = [r for r, _ in br]
+            par = self.s.request(rids[0])["parent"]
+            page = par if par >= 0 else rids[0]
+            assert pseq == self.s.request(page)["seq"]
+            out.append((page, rids))
+        return adm, pre, out
+
+    def update(self, step, acc):
+        self.s.update(step, acc)
+
+    def output(self, rid):
+        return self.s.output(rid)
+
+    def free(self):
+        return self.pool.stats()["free_blocks"]
+
+
+@pytest.mark.parametrize("name", ["sched_small.txt", "sched_multichild.txt"])
+def test_port_golden_run(padoc_lib, name):
+    """The C++ port replays the hand-worked runs directly."""
+    from test_oracle_scheduler import replay
+    replay(PortSched, name)
+
