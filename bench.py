@@ -12,7 +12,13 @@ A step runs both regimes of the hot path on the serving-scale workload:
 `value` is branch-decode attention tokens per second (query tokens of all
 ranks divided by the slowest rank's decode time); the forward's and the
 backward's TFLOP/s and the roofline fractions ride along in the same JSON
-line.
+line.  The same timed loop also runs two smaller decode steps on pages of
+their own and reports them under kernels.branch_decode and kernels.verify:
+  * branch decode over 16 pages (prefix 4809, 8-40 branches, own suffix
+    U[0, 512], one query per branch);
+  * speculative verify over 64 pages (the same shapes, a draft tree of up
+    to 16 nodes per branch), followed by the accept step over every draft
+    node's 151,936 logits.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -233,6 +239,32 @@ def bwd_traffic(units: float):
     return None if a is None or b is None else a + b
 
 
+def decode_report(dec, dw, t_pre: float, t_own: float, hbm: float, tf_sus: float) -> dict:
+    """Per-pass and whole-step figures of one decode / verify step: times,
+    algorithmic bytes (unique KV once per page, own tokens once, the query
+    block, O and LSE) and flops (4 d Hq per query-ancestor pair), the
+    fractions of HBM and sustained tensor peak, and the roofline bound time
+    max(bytes / BW, flops / peak)."""
+    own_b, pre_b, all_b = dec.own_bytes(), dec.prefix_bytes(), dec.unique_kv_bytes()
+    dec_fl = dec.flops()
+    pre_fl = 4.0 * dw.d * dw.Hq * sum(pg.q_len[j] * pg.branch_prefix_len[j] for pg in dw.pages
+                                      for j in range(len(pg.q_len)))
+    own_fl = dec_fl - pre_fl
+    t_dec = t_pre + t_own
+
+    def part(ms, b, fl):
+        gbs, tfs = b / (ms * 1e-3) / 1e9, fl / (ms * 1e-3) / 1e12
+        bound = max(b / (hbm * 1e9), fl / (tf_sus * 1e12)) * 1e3
+        return {"ms": ms, "algorithmic_bytes": b, "algorithmic_flops": fl, "achieved_gbs": gbs,
+                "frac_hbm": gbs / hbm, "achieved_tflops": tfs, "frac_tensor": tfs / tf_sus,
+                "bound_time_ms": bound, "frac_of_bound": bound / ms}
+
+    return {"prefix_pass": part(t_pre, pre_b, pre_fl), "own_pass": part(t_own, own_b, own_fl),
+            "step": dict(part(t_dec, all_b, dec_fl), tokens_per_s=dec.nq / (t_dec * 1e-3),
+                         frac_spec_8tbs=all_b / (t_dec * 1e-3) / 1e9 / 8000.0),
+            "pages": len(dw.pages), "branches": dw.n_branches, "query_tokens": dec.nq}
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -247,6 +279,8 @@ def main() -> int:
                     help="serving (the default bench line); branch and verify are smaller cases for profiling")
     ap.add_argument("--fwd-seqs", type=int, default=8, help="packed 16384-token sequences in the forward")
     ap.add_argument("--vocab", type=int, default=151936, help="vocabulary of the verify workload's accept step")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the 16-page branch decode and 64-page verify steps timed beside the serving step")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -289,17 +323,49 @@ def main() -> int:
         if acc is not None:
             acc.run()
 
+    # Beside the serving step, the same loop times the 16-page branch decode
+    # and the 64-page speculative verify step (attention + accept), each on
+    # its own seeded pages.
+    side = {}
+    if args.workload == "serving" and not args.no_side:
+        bw = wl.branch_decode(seed)
+        side["branch_decode"] = {"w": bw, "dec": harness.Decode(bw, seed=seed + 1, tree=False)}
+        vw = wl.spec_verify(seed)
+        side["verify"] = {"w": vw, "dec": harness.Decode(vw, seed=seed + 2, tree=True),
+                          "acc": harness.Accept([t for pg in vw.pages for t in pg.parents], args.vocab, seed + 3)}
+        for sd in side.values():
+            sd["dec"].plan()
+
+    def side_step(evs):
+        i = 0
+        for name in ("branch_decode", "verify"):
+            if name not in side:
+                continue
+            sd = side[name]
+            evs[i].record(stream)
+            sd["dec"].prefix_pass()
+            evs[i + 1].record(stream)
+            sd["dec"].own_pass()
+            evs[i + 2].record(stream)
+            if "acc" in sd:
+                sd["acc"].run()
+            evs[i + 3].record(stream)
+            i += 4
+
+    n_side_ev = 4 * len(side)
     for _ in range(args.warmup):
         dec.prefix_pass()
         dec.own_pass()
         accept_step()
         fwd.run()
         bwd.run()
+        side_step([torch.cuda.Event() for _ in range(n_side_ev)])
     torch.cuda.synchronize()
     padoc.device_status()
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_side_ev)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.2)
@@ -318,6 +384,7 @@ def main() -> int:
         ev[s][4].record(stream)
         bwd.run()
         ev[s][5].record(stream)
+        side_step(sev[s])
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -329,10 +396,12 @@ def main() -> int:
     t_fwd = sum(e[3].elapsed_time(e[4]) for e in ev) / K
     t_bwd = sum(e[4].elapsed_time(e[5]) for e in ev) / K
     t_dec = t_pre + t_own
-    times = torch.tensor([t_dec, t_fwd, t_pre, t_own, t_acc, t_bwd], dtype=torch.float64, device="cuda")
+    t_side = [sum(e[i].elapsed_time(e[i + 1]) for e in sev) / K for i in range(n_side_ev) if i % 4 != 3]
+    times = torch.tensor([t_dec, t_fwd, t_pre, t_own, t_acc, t_bwd] + t_side, dtype=torch.float64, device="cuda")
     if world > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_dec, t_fwd, t_pre, t_own, t_acc, t_bwd = [float(x) for x in times.tolist()]
+    t_dec, t_fwd, t_pre, t_own, t_acc, t_bwd = [float(x) for x in times.tolist()[:6]]
+    t_side = [float(x) for x in times.tolist()[6:]]
 
     # end to end through the all-in-one C-ABI call, inputs from pinned host memory
     e2e = None
@@ -484,6 +553,24 @@ def main() -> int:
             "vocab": args.vocab, "draft_nodes": acc.nq, "mean_accepted": acc.mean_accepted(),
             "what": "row argmax over every draft node's logits + greedy tree walk (tau 0.75)"}
         line["kernels"]["verify_step"] = {"ms": t_dec + t_acc, "tokens_per_s": nq * world / ((t_dec + t_acc) * 1e-3)}
+    for i, name in enumerate(n for n in ("branch_decode", "verify") if n in side):
+        sd = side[name]
+        t_p, t_o, t_a = t_side[3 * i], t_side[3 * i + 1], t_side[3 * i + 2]
+        rep = decode_report(sd["dec"], sd["w"], t_p, t_o, hbm, tf_sus)
+        rep["workload"] = WORKLOADS[name]
+        if "acc" in sd:
+            a = sd["acc"]
+            a_gbs = a.bytes / (t_a * 1e-3) / 1e9
+            rep["accept"] = {"ms": t_a, "algorithmic_bytes": a.bytes, "achieved_gbs": a_gbs, "frac_hbm": a_gbs / hbm,
+                             "vocab": args.vocab, "draft_nodes": a.nq, "mean_accepted": a.mean_accepted(),
+                             "traffic": traffic_for("accept", a.nq * args.vocab)}
+            t_v = rep["step"]["ms"] + t_a
+            rep["verify_step"] = {"ms": t_v, "tokens_per_s": sd["dec"].nq * world / (t_v * 1e-3),
+                                  "what": "prefix pass + own pass + accept (row argmax, tree walk at tau 0.75)"}
+        line["kernels"][name] = rep
+    if side:
+        # branch decode: prefix + own pass; verify: prefix + own pass + row argmax + tree walk
+        line["gpu_launches"] += (2 * ("branch_decode" in side) + 4 * ("verify" in side)) * K
     if e2e:
         line["e2e"] = e2e
     if cpu:

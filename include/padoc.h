@@ -190,6 +190,15 @@ PADOC_API int padoc_kv_pool_stats(const padoc_kv_pool* pool, int32_t* free_block
 /* Allocates the device block table if needed and uploads changed rows
  * (synchronous with respect to the host tables; copies enqueue on stream). */
 PADOC_API int padoc_kv_pool_sync(padoc_kv_pool* pool, padoc_stream_t stream);
+/* The device that holds the pool's block table (the device current at the
+ * first padoc_kv_pool_sync), or -1 before that.  Decode calls require it to
+ * be the current device and return PADOC_ERR_INVALID otherwise. */
+PADOC_API int padoc_kv_pool_device(const padoc_kv_pool* pool, int32_t* device);
+/* Testing aid, not for normal use: records `device` as the pool's device
+ * without moving anything, so that a machine with one GPU can exercise the
+ * device-mismatch rejection.  Restore the true device before any decode
+ * call is meant to run.  PADOC_ERR_INVALID before the first sync. */
+PADOC_API int padoc_debug_kv_pool_rehome(padoc_kv_pool* pool, int32_t device);
 
 /* ------------------------------------------------------------------------
  * Backward of the packed tree-varlen forward (training; PaDoc, "Training
@@ -498,11 +507,19 @@ PADOC_API int padoc_depths(const int32_t* layout_len, const int32_t* content_len
  *    needs about 10 MiB.
  *  - The pool's device block table must already exist (call
  *    padoc_kv_pool_sync once at set-up); otherwise PADOC_ERR_INVALID.
- *  - No device memory is allocated or freed; the host plan lives on the host
- *    heap.
+ *  - The pool's device (padoc_kv_pool_device) must be the current device;
+ *    otherwise PADOC_ERR_INVALID before any device work.
+ *  - The call allocates and frees no device memory itself; the host plan
+ *    lives on the host heap.
  *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before any
- *    stream capture.
+ *    per device, with that device current) and caches it.  With lazy module
+ *    loading (CUDA_MODULE_LOADING=LAZY, the default) that lookup is also
+ *    the moment the driver loads the library's module on the device and
+ *    reserves the array, so the first call is the one that takes device
+ *    memory.  Make that first call at set-up, before any stream capture and
+ *    before the arena takes the rest of the GPU.  After cudaDeviceReset the
+ *    cached address is stale: do not use the library on that device again
+ *    in the same process (its pools' tables are gone as well).
  *  - All calls share the one array and it keeps the last call's contents.
  *    Nothing in it needs to start at zero: each call writes every byte it
  *    later reads.  Calls whose work overlaps on the GPU (other streams, other

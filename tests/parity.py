@@ -49,3 +49,68 @@ def check_grad(g_gpu, g_ref, dtype="bf16", what=""):
     assert rmax <= lim[0], f"{what}: max error {rmax:.3e} of max|ref|"
     assert rmean <= lim[1], f"{what}: mean error {rmean:.3e} of mean|ref|"
     return float(rmax), float(rmean)
+
+
+# ---------------------------------------------------------------- pooled oracle
+# Whole-page oracle runs at full size take minutes of float64 work, so the
+# rows are dealt out to a pool of spawned processes (spawn, not fork: the
+# parent has already used the GPU).  Each worker memory-maps the inputs from
+# an .npz written by the test and runs the oracle on its rows only.
+
+
+def _load(path):
+    z = np.load(path)
+    return {k: z[k] for k in z.files}
+
+
+def _forward_rows(args):
+    path, pages, rows = args
+    from oracle import tree_attention as ta
+    x = _load(path)
+    O, L = ta.tree_forward(x["q"], x["k"], x["v"], pages, positions=rows)
+    return rows, O[rows], L[:, rows]
+
+
+def _backward_rows(args):
+    path, pages, rows = args
+    from oracle import tree_backward as tb
+    x = _load(path)
+    dQ, dK, dV = tb.tree_backward(x["q"], x["k"], x["v"], x["do"], pages, positions=rows)
+    return rows, dQ[rows], dK, dV
+
+
+def _pool_map(fn, path, pages, rows, n_chunks):
+    import multiprocessing as mp
+    import os
+    rows = list(rows)
+    n_proc = max(1, min(len(os.sched_getaffinity(0)), n_chunks))
+    chunks = [rows[c::n_chunks] for c in range(n_chunks) if rows[c::n_chunks]]
+    with mp.get_context("spawn").Pool(processes=n_proc) as pool:
+        return pool.map(fn, [(path, pages, sorted(c)) for c in chunks])
+
+
+def pooled_forward(path, pages, T, Hq, d, rows=None, n_chunks=64):
+    """The oracle's forward O [T, Hq, d] and LSE [Hq, T] over `rows` (all by
+    default; other rows stay NaN), computed by a process pool."""
+    rows = range(T) if rows is None else rows
+    O = np.full((T, Hq, d), np.nan)
+    L = np.full((Hq, T), np.nan)
+    for r, o, l in _pool_map(_forward_rows, path, pages, rows, n_chunks):
+        O[r] = o
+        L[:, r] = l
+    return O, L
+
+
+def pooled_backward(path, pages, T, Hq, Hkv, d, rows=None, n_chunks=64):
+    """The oracle's dQ (on `rows`), dK and dV (the contributions of those
+    rows: the whole gradient of every key that only they see), computed by a
+    process pool; the chunks' key gradients add."""
+    rows = range(T) if rows is None else rows
+    dQ = np.full((T, Hq, d), np.nan)
+    dK = np.zeros((T, Hkv, d))
+    dV = np.zeros((T, Hkv, d))
+    for r, dq, dk, dv in _pool_map(_backward_rows, path, pages, rows, n_chunks):
+        dQ[r] = dq
+        dK += dk
+        dV += dv
+    return dQ, dK, dV

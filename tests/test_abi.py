@@ -184,6 +184,17 @@ def test_pool_rejects_bad_arguments(padoc_lib):
 FAKE = 1 << 20  # a pointer value nothing dereferences: every call below fails host checks first
 
 
+def test_pool_device_before_sync(padoc_lib):
+    """Before its first sync a pool has no device table: its device reads
+    -1 and the testing relabel is refused (host only; decode calls compare
+    this device with the current one before any launch)."""
+    pool = padoc.KVPool(1 << 20, 1 << 20, 8, Hkv=2, d=128)
+    assert pool.device() == -1
+    with pytest.raises(padoc.PadocError) as e:
+        pool.debug_rehome(1)
+    assert e.value.code == padoc.ERR_INVALID
+
+
 def test_commit_rejects_bad_lists_and_oom_changes_nothing(padoc_lib):
     pool = padoc.KVPool(FAKE, FAKE, 4, Hkv=2, d=128, max_seqs=4, max_blocks_per_seq=8)
     a, b = pool.alloc(0), pool.alloc(0)

@@ -128,3 +128,45 @@ def test_packed_backward_sampled_regions(padoc_lib):
             ref = tb.tree_backward(*host, page, positions=rows)
             for g, rr_, name in zip((b.dq, b.dk, b.dv), ref, ("dq", "dk", "dv")):
                 check_grad(g[a:e].float().cpu().numpy()[rows], rr_[rows], "bf16", f"page {pi} region {r} {name}")
+
+
+def test_packed_backward_whole_page(padoc_lib, tmp_path):
+    """The bench's training workload (8 packed sequences of 16384 tokens) in
+    one backward launch, checked on one whole page: the smallest page that
+    has a prefix, layout and content.  Only a page's own queries see its
+    keys, so the oracle over every query of the page gives every gradient on
+    it, including dK / dV of the prefix keys, which the key-stationary pass
+    accumulates over thousands of queries in dozens of query tiles."""
+    import torch
+    from oracle import tree_attention as ta
+    from parity import pooled_backward
+    from tree_structured_shared_gb300 import harness
+    fw = wl.packed_sequences(0)
+    f = harness.Forward(fw, seed=0)
+    f.run()
+    b = harness.Backward(f, seed=0)
+    b.run()
+    torch.cuda.synchronize()
+    padoc.device_status()
+    starts = np.cumsum([0] + [p.n_tokens for p in fw.pages])
+    cand = [i for i, pg in enumerate(fw.pages) if sum(pg.layout_len) > 0 and sum(pg.content_len) > 0]
+    pi = min(cand, key=lambda i: fw.pages[i].n_tokens)
+    a, e = int(starts[pi]), int(starts[pi + 1])
+    page = [fw.pages[pi]]
+    T = e - a
+    assert fw.pages[pi].prefix_len >= 4000 and T >= 4000
+    host = [x[a:e].float().cpu().numpy() for x in (f.q, f.k, f.v, b.d_o)]
+    path = str(tmp_path / "page.npz")
+    np.savez(path, q=host[0], k=host[1], v=host[2], do=host[3])
+    dQ, dK, dV = pooled_backward(path, page, T, fw.Hq, fw.Hkv, fw.d)
+    got = [g[a:e].float().cpu().numpy() for g in (b.dq, b.dk, b.dv)]
+    ident, _ = ta.packed_layout(page)
+    X = [t for t, x in enumerate(ident) if x[1] == ta.X_KIND]
+    B = [t for t, x in enumerate(ident) if x[1] == ta.B_KIND]
+    assert len(X) >= 4000 and len(B) > 0
+    check_grad(got[0], dQ, "bf16", f"page {pi} dq (all {T} rows)")
+    for g, r, name in ((got[1], dK, "dk"), (got[2], dV, "dv")):
+        check_grad(g, r, "bf16", f"page {pi} {name} (all keys)")
+        check_grad(g[X], r[X], "bf16", f"page {pi} {name} (prefix keys)")
+        check_grad(g[B], r[B], "bf16", f"page {pi} {name} (layout keys)")
+

@@ -40,14 +40,24 @@ def test_tiny_fp32_page(harness):
 
 
 @pytest.mark.parametrize("seed", [0, 1])
-def test_qwen_page_bf16_sampled(harness, seed):
+def test_qwen_page_bf16_every_row(harness, seed, tmp_path):
+    """The Qwen-shaped page (X = 2048, 24 regions, lognormal content) on
+    every row: all tile edges, every region's first layout and content token
+    (where a causal own segment starts) and every ragged tail.  The oracle
+    runs in a pool of spawned processes."""
+    from parity import pooled_forward
     w = wl.qwen_page(seed)
-    rng = np.random.default_rng(seed)
-    T = w.n_tokens
-    # every tile boundary region plus a random sample
-    pos = sorted(set(rng.choice(T, 400, replace=False).tolist()) | {0, 1, 63, 64, 2047, 2048, T - 1})
-    og, lg, O, L = _run(harness, w, seed, positions=pos)
-    check(og, lg, O, L, "bf16", "qwen page")
+    q, k, v = wl.tree_qkv(w, seed)
+    f = harness.Forward(w, q, k, v)
+    o, lse = f.run()
+    import torch
+    torch.cuda.synchronize()
+    padoc.device_status()
+    path = str(tmp_path / "qkv.npz")
+    np.savez(path, q=q, k=k, v=v)
+    O, L = pooled_forward(path, w.pages, w.n_tokens, w.Hq, w.d)
+    check(o.float().cpu().numpy()[: w.n_tokens], lse.cpu().numpy()[:, : w.n_tokens], O, L, "bf16",
+          f"qwen page seed {seed}, all {w.n_tokens} rows")
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])

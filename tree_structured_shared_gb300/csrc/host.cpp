@@ -851,6 +851,19 @@ static int pool_sync(padoc_kv_pool* pool, cudaStream_t stream) {
   return PADOC_OK;
 }
 
+extern "C" int padoc_kv_pool_device(const padoc_kv_pool* pool, int32_t* device) {
+  if (!pool || !device) return fail(PADOC_ERR_INVALID, "kv_pool_device: null argument");
+  *device = pool->d_table ? pool->device : -1;
+  return PADOC_OK;
+}
+
+extern "C" int padoc_debug_kv_pool_rehome(padoc_kv_pool* pool, int32_t device) {
+  if (!pool) return fail(PADOC_ERR_INVALID, "debug_kv_pool_rehome: null pool");
+  if (!pool->d_table) return fail(PADOC_ERR_INVALID, "debug_kv_pool_rehome: the pool has no device table yet");
+  pool->device = device;
+  return PADOC_OK;
+}
+
 extern "C" int padoc_kv_pool_sync(padoc_kv_pool* pool, padoc_stream_t stream) {
   if (!pool) return fail(PADOC_ERR_INVALID, "kv_pool_sync: null pool");
   return pool_sync(pool, reinterpret_cast<cudaStream_t>(stream));
@@ -1173,6 +1186,8 @@ extern "C" int padoc_decode_plan_upload(padoc_decode_plan* plan, void* ws, size_
   int rc = check_ws(plan, ws, ws_bytes);
   if (rc) return rc;
   if (!plan->pool->k || !plan->pool->v) return fail(PADOC_ERR_INVALID, "decode: pool has no storage");
+  rc = padoc::pool_check_device(plan->pool, "decode_plan_upload");
+  if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = pool_sync(plan->pool, st);
   if (rc) return rc;
@@ -1276,6 +1291,16 @@ int set_error(int code, const char* fmt, ...) {
   return fail(code, "%s", buf);
 }
 bool pool_has_device_table(const padoc_kv_pool* pool) { return pool && pool->d_table; }
+int pool_check_device(const padoc_kv_pool* pool, const char* what) {
+  if (!pool || !pool->d_table) return PADOC_OK;
+  int cur = -1;
+  const cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != pool->device)
+    return fail(PADOC_ERR_INVALID, "%s: the pool's block table is on device %d but device %d is current", what,
+                pool->device, cur);
+  return PADOC_OK;
+}
 int32_t pool_num_blocks(const padoc_kv_pool* pool) { return pool ? pool->nb : 0; }
 }  // namespace padoc
 

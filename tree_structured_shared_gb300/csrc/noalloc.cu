@@ -74,6 +74,13 @@ extern "C" int padoc_branch_decode_noalloc(padoc_kv_pool* pool, const padoc_deco
     padoc_decode_plan_free(plan);
     return padoc::set_error(PADOC_ERR_INVALID, "branch_decode_noalloc: null tensor");
   }
+  // the scratch address is looked up for the current device: the pool's
+  // table, the KV blocks and the caller's tensors must live there too
+  rc = padoc::pool_check_device(pool, "branch_decode_noalloc");
+  if (rc) {
+    padoc_decode_plan_free(plan);
+    return rc;
+  }
   void* ws = nullptr;
   rc = scratch_address(&ws);
   if (!rc) rc = padoc_decode_plan_upload(plan, ws, PADOC_NOALLOC_SCRATCH_BYTES, stream);

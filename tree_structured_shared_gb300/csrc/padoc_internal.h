@@ -172,5 +172,8 @@ int set_error(int code, const char* fmt, ...);
 int32_t pool_num_blocks(const padoc_kv_pool* pool);
 // True once the pool's device block table exists (padoc_kv_pool_sync ran).
 bool pool_has_device_table(const padoc_kv_pool* pool);
+// PADOC_OK when the pool has no device table yet or its device is current;
+// else PADOC_ERR_INVALID (message names the call).
+int pool_check_device(const padoc_kv_pool* pool, const char* what);
 
 }  // namespace padoc

@@ -25,8 +25,8 @@ EXPORTED = [
     "padoc_tree_desc_info", "padoc_tree_desc_segments", "padoc_tree_desc_upload",
     "padoc_tree_attn_varlen", "padoc_kv_pool_create", "padoc_kv_pool_destroy", "padoc_kv_alloc",
     "padoc_kv_append", "padoc_kv_fork", "padoc_kv_release", "padoc_kv_seq_info", "padoc_kv_seq_blocks",
-    "padoc_kv_block_refcount", "padoc_kv_pool_stats", "padoc_kv_pool_sync",
-    "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
+    "padoc_kv_block_refcount", "padoc_kv_pool_stats", "padoc_kv_pool_sync", "padoc_kv_pool_device",
+    "padoc_debug_kv_pool_rehome", "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
     "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_upload",
     "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free", "padoc_branch_decode_noalloc",
     "padoc_verify_accept", "padoc_kv_commit", "padoc_draft_index_create", "padoc_draft_index_free",
@@ -100,6 +100,8 @@ def lib() -> C.CDLL:
             "padoc_kv_block_refcount": (C.c_int, [vp, i32, p32]),
             "padoc_kv_pool_stats": (C.c_int, [vp, p32, p32]),
             "padoc_kv_pool_sync": (C.c_int, [vp, vp]),
+            "padoc_kv_pool_device": (C.c_int, [vp, p32]),
+            "padoc_debug_kv_pool_rehome": (C.c_int, [vp, i32]),
             "padoc_branch_decode_ws_size": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, C.POINTER(C.c_size_t)]),
             "padoc_branch_decode": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, vp, vp, vp, vp, vp, vp, f32, vp,
                                               C.c_size_t, vp]),
@@ -309,6 +311,15 @@ class KVPool:
 
     def sync(self, stream=None):
         _check(lib().padoc_kv_pool_sync(self.handle, _stream(stream)))
+
+    def device(self) -> int:
+        d = C.c_int32()
+        _check(lib().padoc_kv_pool_device(self.handle, C.byref(d)))
+        return d.value
+
+    def debug_rehome(self, device: int):
+        """Testing aid (padoc_debug_kv_pool_rehome): relabels the pool's device."""
+        _check(lib().padoc_debug_kv_pool_rehome(self.handle, device))
 
     def reserve(self, seq: int, n_tokens: int):
         _check(lib().padoc_kv_reserve(self.handle, seq, n_tokens))
