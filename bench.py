@@ -557,7 +557,7 @@ def main() -> int:
         sd = side[name]
         t_p, t_o, t_a = t_side[3 * i], t_side[3 * i + 1], t_side[3 * i + 2]
         rep = decode_report(sd["dec"], sd["w"], t_p, t_o, hbm, tf_sus)
-        rep["workload"] = WORKLOADS[name]
+        rep["workload"] = WORKLOADS["branch" if name == "branch_decode" else name]
         if "acc" in sd:
             a = sd["acc"]
             a_gbs = a.bytes / (t_a * 1e-3) / 1e9

@@ -45,6 +45,64 @@ def test_small_decode_groups(harness, G):
     check(og, lg, O, L, "bf16", f"decode G={G}")
 
 
+@pytest.mark.parametrize("G", [1, 4])
+def test_small_verify_groups(harness, G):
+    """Draft trees with G = 1 (keys-on-M own pass, 16 rows per unit) and
+    G = 4 (the rows-on-M tensor-core own pass)."""
+    w = wl.small_decode(40 + G, n_pages=3, max_prefix=500, max_branches=5, max_own=300, Hq=2 * G, Hkv=2)
+    og, lg, O, L = _decode(harness, w, 40 + G)
+    check(og, lg, O, L, "bf16", f"verify G={G}")
+
+
+def test_verify_long_prefix_many_chunks(harness):
+    """Long page prefixes in a small batch: the plan splits each page's
+    prefix into several chunks, so the own pass merges several partial
+    results per row (besides draft trees and ragged per-branch prefixes)."""
+    w = wl.small_decode(60, n_pages=2, max_prefix=4500, max_branches=4, max_own=300, Hq=4, Hkv=2)
+    og, lg, O, L = _decode(harness, w, 60)
+    check(og, lg, O, L, "bf16", "verify, several prefix chunks per page")
+
+
+def test_verify_rows_major_own_pass(padoc_lib, tmp_path):
+    """The rows-on-M tensor-core own pass (PADOC_OWN_KERNEL=rows, read once
+    per process, so in a child) on the same draft-tree pages as the default
+    keys-on-M pass: both against the oracle."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = tmp_path / "o.npz"
+    code = (
+        "import sys, numpy as np, torch; sys.path.insert(0, %r)\n"
+        "from tree_structured_shared_gb300 import harness, padoc, workloads as wl\n"
+        "w = wl.small_decode(3, n_pages=4, max_prefix=700, max_branches=6, max_own=300, Hq=4, Hkv=2)\n"
+        "d = harness.Decode(w, wl.decode_values(w, 3), tree=True); o, l = d.run(); torch.cuda.synchronize()\n"
+        "padoc.device_status()\n"
+        "np.savez(%r, o=o.float().cpu().numpy()[:w.n_queries], l=l.cpu().numpy()[:w.n_queries])\n"
+    ) % (root, str(out))
+    env = dict(os.environ, PADOC_OWN_KERNEL="rows")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    got = np.load(out)
+    w = wl.small_decode(3, n_pages=4, max_prefix=700, max_branches=6, max_own=300, Hq=4, Hkv=2)
+    O, L = ta.branch_decode(w, wl.decode_values(w, 3), tree=True)
+    check(got["o"], got["l"], O, L, "bf16", "rows-major own pass")
+
+
+def test_verify_repeat_runs_bit_identical(harness):
+    """The full 64-page verify batch run repeatedly: any ordering race in
+    the pipelines shows up as a difference between runs."""
+    import torch
+    w = wl.spec_verify(1)
+    d = harness.Decode(w, seed=1, tree=True)
+    o0, l0 = [x.clone() for x in d.run()]
+    for _ in range(3):
+        o, l = d.run()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    padoc.device_status()
+
+
 def test_chain_block_without_tree(harness):
     w = wl.small_decode(9, n_pages=2, max_prefix=300, max_branches=4, max_own=60, verify=True, Hq=4, Hkv=2)
     og, lg, O, L = _decode(harness, w, 9, tree=False)

@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpadoc.so")
-SOURCES = ["host.cpp", "attn_tc.cu", "cuda_core.cu", "accept.cu", "bwd_core.cu", "attn_bwd_tc.cu", "noalloc.cu", "draft.cpp", "sched.cpp"]
+SOURCES = ["host.cpp", "attn_tc.cu", "cuda_core.cu", "accept.cu", "bwd_core.cu", "attn_bwd_tc.cu", "noalloc.cu", "own_kmajor.cu", "draft.cpp", "sched.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xcompiler", "-Wall"]
 

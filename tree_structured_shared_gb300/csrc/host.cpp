@@ -1259,8 +1259,19 @@ extern "C" int padoc_decode_own_pass(const padoc_decode_plan* plan, const void* 
   if (!plan->pool->d_table) return fail(PADOC_ERR_INVALID, "decode_own_pass: plan was not uploaded");
   const DecodeArgs a = decode_args(plan, q, k_new, v_new, tree_bits, o, lse, scale, ws);
   std::string err;
-  rc = plan->pl.tc_own ? launch_decode_own_tc(a, reinterpret_cast<cudaStream_t>(stream), &err)
-                       : launch_decode_own(a, reinterpret_cast<cudaStream_t>(stream), &err);
+  // Several query rows per (branch, kv head) (verify): tensor cores.  With
+  // Hq / Hkv <= 2 a unit has at most 32 rows and the keys go on the MMA's M
+  // side; PADOC_OWN_KERNEL=rows selects the rows-on-M engine instead (the
+  // one used for larger groups).
+  static const bool rows_major = std::getenv("PADOC_OWN_KERNEL") &&
+                                 std::string(std::getenv("PADOC_OWN_KERNEL")) == "rows";
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!plan->pl.tc_own)
+    rc = launch_decode_own(a, st, &err);
+  else if (a.group <= 2 && !rows_major)
+    rc = launch_decode_own_kmajor(a, st, &err);
+  else
+    rc = launch_decode_own_tc(a, st, &err);
   if (rc) return fail(rc, "decode_own_pass: %s", err.c_str());
   return PADOC_OK;
 }
@@ -1355,11 +1366,12 @@ extern "C" int padoc_depths(const int32_t* layout_len, const int32_t* content_le
 }
 
 extern "C" int padoc_device_status(padoc_stream_t stream) {
-  unsigned w = 0, wb = 0;
+  unsigned w = 0, wb = 0, wo = 0;
   int rc = read_and_clear_tc_error(reinterpret_cast<cudaStream_t>(stream), &w);
   if (!rc) rc = read_and_clear_bwd_error(reinterpret_cast<cudaStream_t>(stream), &wb);
+  if (!rc) rc = read_and_clear_own_error(reinterpret_cast<cudaStream_t>(stream), &wo);
   if (rc) return fail(rc, "device_status: could not read the device error word");
-  w |= wb;
+  w |= wb | wo;
   if (w) return fail(PADOC_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (site mask 0x%x)", w);
   return PADOC_OK;
 }

@@ -140,6 +140,8 @@ int launch_fwd_f32(const FwdArgs& a, cudaStream_t s, std::string* err);
 int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err);
 int launch_decode_own(const DecodeArgs& a, cudaStream_t s, std::string* err);
 int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err);
+// Verify own pass with keys on the MMA's M side (Hq / Hkv of 1 or 2).
+int launch_decode_own_kmajor(const DecodeArgs& a, cudaStream_t s, std::string* err);
 int launch_kv_append(void* k_pool, void* v_pool, const int32_t* table_row, int32_t first_own,
                      int32_t n, int32_t Hkv, int32_t d, const void* k, const void* v,
                      cudaStream_t s, std::string* err);
@@ -158,6 +160,7 @@ int read_and_clear_bwd_error(cudaStream_t s, unsigned* word);
 
 // Device error words (set by kernels that give up a bounded wait).
 int read_and_clear_tc_error(cudaStream_t s, unsigned* word);
+int read_and_clear_own_error(cudaStream_t s, unsigned* word);
 
 // Driver entry point for tensor-map encoding (resolved through the runtime).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
