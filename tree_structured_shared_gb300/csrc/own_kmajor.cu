@@ -461,6 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         row_lpre(rb)[r] = lpre;
         row_prow(rb)[r] = static_cast<int32_t>(prow0);
         row_share(rb)[r] = pg.n_chunks > 0 ? fast_exp2(l0 - lpre) : 0.f;
+        if (pg.n_chunks > 0) {
+          // the epilogue stages this 512-byte partial row: bring it to L2 now
+          const char* row = reinterpret_cast<const char*>(p.part_o + prow0 * kHeadDim);
+          for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + k * 128));
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_ROW_FULL + rb));
@@ -531,11 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; j < w.n_tiles; ++j, ++kt) {
         const int sb = kt & 1;
+        // a failed wait here is voted on with the P buffer's below (reading
+        // an unfinished S^T only gives values that are thrown away)
         const bool ok_s = __all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_S_FULL + sb), (kt >> 1) & 1, abort));
-        if (bar_or_all(!ok_s)) {
-          failed = true;
-          break;
-        }
         tc_fence_after();
         float x[kHalfRows];
         {
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // released the buffer
         const bool ok_p =
             kt < 2 || __all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_P_FREE + sb), ((kt >> 1) & 1) ^ 1, abort));
-        if (bar_or_all(!ok_p || late)) {
+        if (bar_or_all(!ok_s || !ok_p || late)) {
           failed = true;
           break;
         }
