@@ -530,6 +530,18 @@ PADOC_API int padoc_branch_decode_noalloc(padoc_kv_pool* pool, const padoc_decod
                                           const uint16_t* tree_bits, void* o, float* lse, float scale,
                                           padoc_stream_t stream);
 
+/* Testing aid, not for normal use: sets, on the current device, the longest
+ * time (nanoseconds) one wait of the verify own pass with keys on the MMA's
+ * M side may take before the kernel gives up and reports
+ * PADOC_ERR_DEVICE_TIMEOUT through padoc_device_status; 0 restores the
+ * default of 2 s.  It applies to that kernel only: when one of its roles
+ * gives up, the others leave their loops, its TMA producers wait for the
+ * copies they issued and its MMA thread for its products before the CTA
+ * releases tensor memory and exits, so a wait that runs out leaves the GPU
+ * usable for the next call (HPD-Parsing's failure detection has no GPU-side
+ * counterpart; this serves tests of the abort path). */
+PADOC_API int padoc_debug_set_wait_limit(uint64_t ns);
+
 /* Reports and clears the device error word of the current device: 0 when no
  * kernel has given up a wait since the last call, else PADOC_ERR_DEVICE_TIMEOUT
  * with the failing site in the message. */

@@ -47,6 +47,9 @@
 namespace padoc {
 
 __device__ unsigned int g_own_err;
+// Longest time one wait of this kernel may take before it gives up
+// (nanoseconds of the global timer); settable for tests, read at launch.
+__device__ unsigned long long g_own_wait_limit_ns = ptx::kWaitLimitNs;
 
 namespace {
 
@@ -139,7 +142,27 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned site) 
   atomicOr(&g_own_err, site);
 }
 
-// A wait that ignores the abort flag but keeps the time limit: used at exit
+// The pipeline's waits, with the limit read at launch.
+__device__ __forceinline__ bool wait_l(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer() - t0 > limit) return false;
+  }
+}
+__device__ __forceinline__ bool wait_relaxed_l(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit) {
+  if (mbar_try_wait_relaxed(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  while (true) {
+    if (mbar_try_wait_relaxed(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer() - t0 > limit) return false;
+  }
+}
+
+// A wait that ignores the abort flag but keeps the default time limit: used at exit
 // to let copies and products already issued land before the CTA leaves.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   int never = 0;
@@ -239,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const int G = p.group;
+  const uint64_t wlim = g_own_wait_limit_ns;
   const int gsh = G == 2 ? 1 : 0;  // row r is query token r >> gsh, head r & gsh of the group (G is 1 or 2)
 
   if (threadIdx.x == 0) {
@@ -300,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch(u + gridDim.x);
       if (is_k) {
         const int qb = iu & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY + qb), ((iu >> 1) & 1) ^ 1, abort))) {
+        if (!__all_sync(0xffffffffu, wait_l(bar(B_Q_EMPTY + qb), ((iu >> 1) & 1) ^ 1, abort, wlim))) {
           failed = true;
           break;
         }
@@ -318,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_own_blocks = (w.own_len + 15) >> 4;
       for (int j = 0; j < w.n_tiles; ++j) {
         const int st = kt % kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(b_empty + st), ((kt / kStages) & 1) ^ 1, abort))) {
+        if (!__all_sync(0xffffffffu, wait_l(bar(b_empty + st), ((kt / kStages) & 1) ^ 1, abort, wlim))) {
           failed = true;
           break;
         }
@@ -363,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool failed = false;
       auto issue_s = [&](uint32_t qaddr) -> bool {
         const int st = kt_s % kStages, sb = kt_s & 1;
-        if (!mbar_wait_relaxed(bar(B_K_FULL + st), (kt_s / kStages) & 1, abort)) return false;
-        if (!mbar_wait_relaxed(bar(B_S_FREE + sb), ((kt_s >> 1) & 1) ^ 1, abort)) return false;
+        if (!wait_relaxed_l(bar(B_K_FULL + st), (kt_s / kStages) & 1, abort, wlim)) return false;
+        if (!wait_relaxed_l(bar(B_S_FREE + sb), ((kt_s >> 1) & 1) ^ 1, abort, wlim)) return false;
         tc_fence_after();
         const uint64_t d_k = sdesc_sw128(sbase + SM_K + st * 2 * kKHalf, 16, 1024);
         const uint64_t d_q = sdesc_sw128(qaddr, 16, 1024);
@@ -384,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit w = w_next;
         if (u + static_cast<int>(gridDim.x) < p.n_units) w_next = load_unit(p, u + gridDim.x);
         const int qb = iu & 1, ob = iu & 1;
-        if (!mbar_wait_relaxed(bar(B_Q_FULL + qb), (iu >> 1) & 1, abort)) { failed = true; break; }
+        if (!wait_relaxed_l(bar(B_Q_FULL + qb), (iu >> 1) & 1, abort, wlim)) { failed = true; break; }
         const uint32_t qaddr = sbase + SM_Q + qb * 2 * kRHalf;
         if (!issue_s(qaddr)) { failed = true; break; }
         for (int j = 0; j < w.n_tiles; ++j) {
@@ -394,9 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(B_Q_EMPTY + qb));  // every S^T of the unit is issued
           }
           const int st = kt_p % kStages, pb = kt_p & 1;
-          if (!mbar_wait_relaxed(bar(B_V_FULL + st), (kt_p / kStages) & 1, abort) ||
-              !mbar_wait_relaxed(bar(B_P_FULL + pb), (kt_p >> 1) & 1, abort) ||
-              (j == 0 && !mbar_wait_relaxed(bar(B_O_FREE + ob), ((iu >> 1) & 1) ^ 1, abort))) {
+          if (!wait_relaxed_l(bar(B_V_FULL + st), (kt_p / kStages) & 1, abort, wlim) ||
+              !wait_relaxed_l(bar(B_P_FULL + pb), (kt_p >> 1) & 1, abort, wlim) ||
+              (j == 0 && !wait_relaxed_l(bar(B_O_FREE + ob), ((iu >> 1) & 1) ^ 1, abort, wlim))) {
             failed = true;
             break;
           }
@@ -432,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = load_unit(p, u);
       const DecPage pg = p.pages[w.page];
       const int rb = iu & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ROW_FREE + rb), ((iu >> 1) & 1) ^ 1, abort))) {
+      if (!__all_sync(0xffffffffu, wait_l(bar(B_ROW_FREE + rb), ((iu >> 1) & 1) ^ 1, abort, wlim))) {
         failed = true;
         break;
       }
@@ -505,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ob = iu & 1, rb = iu & 1;
       // bit i: row r0 + i of the unit exists
       const uint32_t my_rows = w.rows - r0 >= 16 ? 0xffffu : (w.rows > r0 ? (1u << (w.rows - r0)) - 1u : 0u);
-      const bool ok_r = __all_sync(0xffffffffu, mbar_wait(bar(B_ROW_FULL + rb), (iu >> 1) & 1, abort));
+      const bool ok_r = __all_sync(0xffffffffu, wait_l(bar(B_ROW_FULL + rb), (iu >> 1) & 1, abort, wlim));
       if (bar_or_all(!ok_r)) {
         failed = true;
         break;
@@ -538,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sb = kt & 1;
         // a failed wait here is voted on with the P buffer's below (reading
         // an unfinished S^T only gives values that are thrown away)
-        const bool ok_s = __all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_S_FULL + sb), (kt >> 1) & 1, abort));
+        const bool ok_s = __all_sync(0xffffffffu, wait_relaxed_l(bar(B_S_FULL + sb), (kt >> 1) & 1, abort, wlim));
         tc_fence_after();
         float x[kHalfRows];
         {
@@ -588,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O^T (lane t = head dim t) holds sums against the old maxima:
             // rescale this half's columns once P V of the previous tile ran
             const uint32_t q = kt - 1;
-            late = !__all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_P_FREE + (q & 1)), (q >> 1) & 1, abort));
+            late = !__all_sync(0xffffffffu, wait_relaxed_l(bar(B_P_FREE + (q & 1)), (q >> 1) & 1, abort, wlim));
           }
           if (j > 0 && any_rescale && !late) {
             tc_fence_after();
@@ -611,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K-major with the 128-byte swizzle), once P V two tiles back has
         // released the buffer
         const bool ok_p =
-            kt < 2 || __all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_P_FREE + sb), ((kt >> 1) & 1) ^ 1, abort));
+            kt < 2 || __all_sync(0xffffffffu, wait_relaxed_l(bar(B_P_FREE + sb), ((kt >> 1) & 1) ^ 1, abort, wlim));
         if (bar_or_all(!ok_s || !ok_p || late)) {
           failed = true;
           break;
@@ -639,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // instruction fetches of big unrolled blocks cost.  Each row half
       // handles its own rows.
       prefetch(u + gridDim.x);
-      const bool ok_e = __all_sync(0xffffffffu, mbar_wait_relaxed(bar(B_O_FULL + ob), (iu >> 1) & 1, abort));
+      const bool ok_e = __all_sync(0xffffffffu, wait_relaxed_l(bar(B_O_FULL + ob), (iu >> 1) & 1, abort, wlim));
       if (bar_or_all(!ok_e)) {
         failed = true;
         break;
@@ -824,6 +848,18 @@ int launch_decode_own_kmajor(const DecodeArgs& a, cudaStream_t s, std::string* e
   }
   return PADOC_OK;
 }
+
+}  // namespace padoc
+
+extern "C" int padoc_debug_set_wait_limit(uint64_t ns) {
+  const unsigned long long v = ns ? ns : padoc::ptx::kWaitLimitNs;
+  const cudaError_t e = cudaMemcpyToSymbol(padoc::g_own_wait_limit_ns, &v, sizeof(v));
+  if (e != cudaSuccess)
+    return padoc::set_error(PADOC_ERR_CUDA, "debug_set_wait_limit: %s", cudaGetErrorString(e));
+  return PADOC_OK;
+}
+
+namespace padoc {
 
 int read_and_clear_own_error(cudaStream_t s, unsigned* word) {
   unsigned zero = 0;

@@ -26,7 +26,7 @@ EXPORTED = [
     "padoc_tree_attn_varlen", "padoc_kv_pool_create", "padoc_kv_pool_destroy", "padoc_kv_alloc",
     "padoc_kv_append", "padoc_kv_fork", "padoc_kv_release", "padoc_kv_seq_info", "padoc_kv_seq_blocks",
     "padoc_kv_block_refcount", "padoc_kv_pool_stats", "padoc_kv_pool_sync", "padoc_kv_pool_device",
-    "padoc_debug_kv_pool_rehome", "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
+    "padoc_debug_kv_pool_rehome", "padoc_debug_set_wait_limit", "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
     "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_upload",
     "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free", "padoc_branch_decode_noalloc",
     "padoc_verify_accept", "padoc_kv_commit", "padoc_draft_index_create", "padoc_draft_index_free",
@@ -102,6 +102,7 @@ def lib() -> C.CDLL:
             "padoc_kv_pool_sync": (C.c_int, [vp, vp]),
             "padoc_kv_pool_device": (C.c_int, [vp, p32]),
             "padoc_debug_kv_pool_rehome": (C.c_int, [vp, i32]),
+            "padoc_debug_set_wait_limit": (C.c_int, [C.c_uint64]),
             "padoc_branch_decode_ws_size": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, C.POINTER(C.c_size_t)]),
             "padoc_branch_decode": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, vp, vp, vp, vp, vp, vp, f32, vp,
                                               C.c_size_t, vp]),
@@ -566,3 +567,10 @@ def depths(layout_len: Sequence[int], content_len: Sequence[int]):
 
 def device_status(stream=None):
     _check(lib().padoc_device_status(_stream(stream)))
+
+
+def debug_set_wait_limit(ns: int):
+    """Testing aid (padoc_debug_set_wait_limit): the wait limit of the
+    verify own pass's keys-on-M kernel on the current device; 0 restores
+    the default."""
+    _check(lib().padoc_debug_set_wait_limit(int(ns)))
