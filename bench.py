@@ -558,6 +558,17 @@ def main() -> int:
         t_p, t_o, t_a = t_side[3 * i], t_side[3 * i + 1], t_side[3 * i + 2]
         rep = decode_report(sd["dec"], sd["w"], t_p, t_o, hbm, tf_sus)
         rep["workload"] = WORKLOADS["branch" if name == "branch_decode" else name]
+        sw = sd["w"]
+        own_units = sum(sum(pg.own_len) for pg in sw.pages)
+        pre_units = sum(max(pg.branch_prefix_len or [0]) for pg in sw.pages)
+        if name == "verify":
+            rep["own_pass"]["kernel"] = "own_kmajor_kernel"
+            rep["own_pass"]["traffic"] = traffic_for("own_kmajor_verify", own_units)
+            rep["prefix_pass"]["traffic"] = traffic_for("prefix_pass_verify", pre_units)
+        else:
+            rep["own_pass"]["kernel"] = "own_pass_kernel"
+            rep["own_pass"]["traffic"] = traffic_for("own_pass", own_units)
+            rep["prefix_pass"]["traffic"] = traffic_for("prefix_pass", pre_units)
         if "acc" in sd:
             a = sd["acc"]
             a_gbs = a.bytes / (t_a * 1e-3) / 1e9

@@ -138,12 +138,13 @@ struct Unit {
 
 __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
   Unit w;
-  // forward: head-major, so the CTAs at work at one time share one kv head's
-  // K/V (a working set that stays in L2); decode: the heads of one item
-  // together
-  const int n_it = p.mode == MODE_FWD ? p.plan.n_items : 0;
-  w.g = p.mode == MODE_FWD ? u / n_it : u % p.Hkv;
-  const int item = p.mode == MODE_FWD ? u % n_it : u / p.Hkv;
+  // forward and prefix pass: head-major, so the CTAs at work at one time
+  // share one kv head's K/V (forward: a working set that stays in L2; prefix
+  // pass: a page's row tiles, adjacent items, read its prefix together);
+  // own pass: the heads of one branch together
+  const int n_it = p.mode == MODE_FWD ? p.plan.n_items : (p.mode == MODE_PREFIX ? p.n_units / p.Hkv : 0);
+  w.g = p.mode == MODE_OWN ? u % p.Hkv : u / n_it;
+  const int item = p.mode == MODE_OWN ? u / p.Hkv : u % n_it;
   if (p.mode == MODE_FWD) {
     const FwdItem it = p.plan.items[item];
     const QSeg qs = p.plan.qsegs[it.qseg];
