@@ -54,19 +54,36 @@ def test_small_verify_groups(harness, G):
     check(og, lg, O, L, "bf16", f"verify G={G}")
 
 
-def test_verify_long_prefix_many_chunks(harness):
-    """Long page prefixes in a small batch: the plan splits each page's
-    prefix into several chunks, so the own pass merges several partial
-    results per row (besides draft trees and ragged per-branch prefixes)."""
+def test_verify_long_prefix_one_chunk(harness):
+    """Page prefixes up to 4500 tokens (at most 36 key tiles) with draft
+    trees and ragged per-branch prefixes: the fused verify pass walks each
+    page's whole prefix as one chunk, then the own suffixes and the query
+    block."""
     w = wl.small_decode(60, n_pages=2, max_prefix=4500, max_branches=4, max_own=300, Hq=4, Hkv=2)
     og, lg, O, L = _decode(harness, w, 60)
+    check(og, lg, O, L, "bf16", "verify, long prefixes in one chunk")
+
+
+def test_verify_prefix_above_one_chunk(harness):
+    """A page prefix of 6000 tokens (47 key tiles, above the 40 of one
+    chunk): the step runs as two passes, the prefix split into several
+    chunks whose partial results the own pass merges."""
+    rng = np.random.default_rng(61)
+    pages = []
+    for P in (6000, 1300):
+        N = 5
+        bpl = rng.integers(0, P, N).tolist()
+        bpl[0] = P
+        parents = [wl.draft_tree(rng, max_nodes=16) for _ in range(N)]
+        pages.append(wl.DecodePage(P, bpl, rng.integers(0, 300, N).tolist(), [len(t) for t in parents], parents))
+    w = wl.DecodeWorkload("long_prefix", pages, 4, 2, 128, 1.0)
+    og, lg, O, L = _decode(harness, w, 61)
     check(og, lg, O, L, "bf16", "verify, several prefix chunks per page")
 
 
-def test_verify_rows_major_own_pass(padoc_lib, tmp_path):
-    """The rows-on-M tensor-core own pass (PADOC_OWN_KERNEL=rows, read once
-    per process, so in a child) on the same draft-tree pages as the default
-    keys-on-M pass: both against the oracle."""
+def _child_verify(tmp_path, env_over, seed=3):
+    """One small draft-tree verify batch run in a child process under the
+    given environment (the kernel choices are read once per process)."""
     import os
     import subprocess
     import sys
@@ -75,18 +92,32 @@ def test_verify_rows_major_own_pass(padoc_lib, tmp_path):
     code = (
         "import sys, numpy as np, torch; sys.path.insert(0, %r)\n"
         "from tree_structured_shared_gb300 import harness, padoc, workloads as wl\n"
-        "w = wl.small_decode(3, n_pages=4, max_prefix=700, max_branches=6, max_own=300, Hq=4, Hkv=2)\n"
-        "d = harness.Decode(w, wl.decode_values(w, 3), tree=True); o, l = d.run(); torch.cuda.synchronize()\n"
+        "w = wl.small_decode(%d, n_pages=4, max_prefix=700, max_branches=6, max_own=300, Hq=4, Hkv=2)\n"
+        "d = harness.Decode(w, wl.decode_values(w, %d), tree=True); o, l = d.run(); torch.cuda.synchronize()\n"
         "padoc.device_status()\n"
         "np.savez(%r, o=o.float().cpu().numpy()[:w.n_queries], l=l.cpu().numpy()[:w.n_queries])\n"
-    ) % (root, str(out))
-    env = dict(os.environ, PADOC_OWN_KERNEL="rows")
+    ) % (root, seed, seed, str(out))
+    env = dict(os.environ, **env_over)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     got = np.load(out)
-    w = wl.small_decode(3, n_pages=4, max_prefix=700, max_branches=6, max_own=300, Hq=4, Hkv=2)
-    O, L = ta.branch_decode(w, wl.decode_values(w, 3), tree=True)
-    check(got["o"], got["l"], O, L, "bf16", "rows-major own pass")
+    w = wl.small_decode(seed, n_pages=4, max_prefix=700, max_branches=6, max_own=300, Hq=4, Hkv=2)
+    O, L = ta.branch_decode(w, wl.decode_values(w, seed), tree=True)
+    return got["o"], got["l"], O, L
+
+
+def test_verify_two_pass_keys_on_m(padoc_lib, tmp_path):
+    """The same verify batch as two passes (PADOC_VERIFY_FUSED=0): the
+    prefix pass, then the keys-on-M own pass that merges its partials."""
+    og, lg, O, L = _child_verify(tmp_path, {"PADOC_VERIFY_FUSED": "0"})
+    check(og, lg, O, L, "bf16", "two-pass verify, keys-on-M own pass")
+
+
+def test_verify_rows_major_own_pass(padoc_lib, tmp_path):
+    """The rows-on-M tensor-core own pass (two passes, PADOC_OWN_KERNEL=rows)
+    on the same draft-tree pages."""
+    og, lg, O, L = _child_verify(tmp_path, {"PADOC_VERIFY_FUSED": "0", "PADOC_OWN_KERNEL": "rows"})
+    check(og, lg, O, L, "bf16", "rows-major own pass")
 
 
 def test_verify_repeat_runs_bit_identical(harness):

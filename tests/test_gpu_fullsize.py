@@ -85,3 +85,27 @@ def test_packed_forward_sampled_rows(harness):
         og = o[a:b].float().cpu().numpy()[rows]
         lg = lse[:, a:b].cpu().numpy()[:, rows]
         check(og, lg, O[rows], L[:, rows], "bf16", f"packed page {pi}")
+
+
+def test_packed_forward_whole_page(harness, tmp_path):
+    """8 packed sequences of 16384 tokens in one launch, checked on every row
+    of one whole page (the smallest with a prefix, layout and content), so
+    every region boundary of the page, where a causal own segment starts,
+    and every tile edge is covered.  The oracle runs in a spawned pool."""
+    import torch
+    from parity import pooled_forward
+    fw = wl.packed_sequences(0)
+    f = harness.Forward(fw, seed=0)
+    o, lse = f.run()
+    torch.cuda.synchronize()
+    padoc.device_status()
+    starts = np.cumsum([0] + [p.n_tokens for p in fw.pages])
+    cand = [i for i, pg in enumerate(fw.pages) if sum(pg.layout_len) > 0 and sum(pg.content_len) > 0]
+    pi = min(cand, key=lambda i: fw.pages[i].n_tokens)
+    a, b = int(starts[pi]), int(starts[pi + 1])
+    host = [x[a:b].float().cpu().numpy() for x in (f.q, f.k, f.v)]
+    path = str(tmp_path / "page.npz")
+    np.savez(path, q=host[0], k=host[1], v=host[2])
+    O, L = pooled_forward(path, [fw.pages[pi]], b - a, fw.Hq, fw.d)
+    check(o[a:b].float().cpu().numpy(), lse[:, a:b].cpu().numpy(), O, L, "bf16", f"packed page {pi}, all rows")
+

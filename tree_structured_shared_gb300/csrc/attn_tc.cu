@@ -16,6 +16,14 @@
 //                the page's shared prefix blocks, read from HBM once for all
 //                branches (HPD-Parsing: forked branches share the prefix KV
 //                with zero copy).  Writes normalised partial O and LSE.
+//   MODE_OWN     own pass of a verify step: rows are the query rows of one
+//                branch; key tiles are its own cached suffix and its query
+//                block; merges with the prefix partials into O and LSE.
+//   MODE_VERIFY  a verify step in one pass: rows as in MODE_PREFIX; key
+//                tiles are the page's prefix (one chunk), then the own
+//                suffix of each branch the rows belong to (visible to that
+//                branch's rows only), then one tile of the query-block keys
+//                (visible by branch and draft-tree mask).  Writes O and LSE.
 //
 // Roles (224 threads):
 //   warps 0-3  softmax: thread r owns TMEM lane r = query row r.  Reads S
@@ -57,7 +65,7 @@ namespace {
 
 using namespace ptx;
 
-enum { MODE_FWD = 0, MODE_PREFIX = 1, MODE_OWN = 2 };
+enum { MODE_FWD = 0, MODE_PREFIX = 1, MODE_OWN = 2, MODE_VERIFY = 3 };
 
 constexpr int kStages = 3;  // K and V tile rings
 constexpr int kSBufs = 3;   // S / P tiles in tensor memory
@@ -123,6 +131,7 @@ struct Params {
   // own pass
   const DecBranch* branches;
   const uint16_t* tree_bits;
+  const int32_t* q_branch;
 };
 
 // The work unit as seen by every role (computed identically by each).
@@ -134,6 +143,8 @@ struct Unit {
   int32_t page, tile, rows, row_base, k_begin, k_end, seq, q_first;
   // own
   int32_t own_len, n_shared, q_len, q_in_page;
+  // fused verify
+  int32_t b_first, b_count, tok_lo;
 };
 
 __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
@@ -142,7 +153,7 @@ __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
   // share one kv head's K/V (forward: a working set that stays in L2; prefix
   // pass: a page's row tiles, adjacent items, read its prefix together);
   // own pass: the heads of one branch together
-  const int n_it = p.mode == MODE_FWD ? p.plan.n_items : (p.mode == MODE_PREFIX ? p.n_units / p.Hkv : 0);
+  const int n_it = p.mode == MODE_FWD ? p.plan.n_items : (p.mode == MODE_OWN ? 0 : p.n_units / p.Hkv);
   w.g = p.mode == MODE_OWN ? u % p.Hkv : u / n_it;
   const int item = p.mode == MODE_OWN ? u / p.Hkv : u % n_it;
   if (p.mode == MODE_FWD) {
@@ -174,6 +185,9 @@ __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
     w.k_end = min(pg.P, w.k_begin + pg.chunk_tokens);
     w.seq = pg.seq;
     w.q_first = pg.q_first;
+    w.b_first = it.b_first;
+    w.b_count = it.b_count;
+    w.tok_lo = it.tok_lo;
   }
   return w;
 }
@@ -199,7 +213,32 @@ __device__ __forceinline__ bool seg_setup(const Params& p, const Unit& w, TileIt
   return false;
 }
 
+// Fused verify: segment 0 is the prefix chunk, segments 1 .. b_count the own
+// suffixes of the unit's branches, segment b_count + 1 the query-block tile.
+__device__ __forceinline__ bool verify_setup(const Params& p, const Unit& w, TileIter& t) {
+  while (t.s < t.s_end) {
+    t.ks = 0;
+    if (t.s == 0) {
+      t.ks = w.k_begin;
+      t.end = w.k_end;
+    } else if (t.s <= w.b_count) {
+      t.end = p.branches[w.b_first + t.s - 1].own_len;
+    } else {
+      t.end = 1;
+    }
+    if (t.ks < t.end) return true;
+    ++t.s;
+  }
+  return false;
+}
+
 __device__ __forceinline__ bool tiles_begin(const Params& p, const Unit& w, TileIter& t) {
+  t.causal = 0;
+  if (p.mode == MODE_VERIFY) {
+    t.s = 0;
+    t.s_end = w.b_count + 2;
+    return verify_setup(p, w, t);
+  }
   if (p.mode == MODE_FWD) {
     t.s = w.kv_first;
     t.s_end = w.kv_first + w.kv_count;
@@ -229,6 +268,10 @@ __device__ __forceinline__ bool tiles_next(const Params& p, const Unit& w, TileI
   if (p.mode == MODE_FWD) {
     ++t.s;
     return seg_setup(p, w, t);
+  }
+  if (p.mode == MODE_VERIFY) {
+    ++t.s;
+    return verify_setup(p, w, t);
   }
   if (p.mode == MODE_OWN && t.s == 0) {
     t.s = 1;
@@ -332,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < 2; ++h) tma_load_4d(sbase + SM_Q + h * kHalf, &tm_q, bar(B_QK0_FULL), h * 64, 0, w.g, q0);
           }
         }
-        if (MODE == MODE_PREFIX) {
+        if (MODE == MODE_PREFIX || MODE == MODE_VERIFY) {
           // block ids of the whole chunk, read once per unit and shared with warp 6
           if (!__all_sync(0xffffffffu, mbar_wait(bar(B_IDS_FREE), (item_it & 1) ^ 1, abort))) { failed = true; break; }
           const int n_ids = (w.k_end - w.k_begin + 15) >> 4;
@@ -341,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_IDS_READY));
         }
-      } else if (MODE == MODE_PREFIX) {
+      } else if (MODE == MODE_PREFIX || MODE == MODE_VERIFY) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_IDS_READY), item_it & 1, abort))) { failed = true; break; }
       }
       const uint32_t it0 = it;  // number of the unit's first tile
@@ -369,12 +412,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < 2; ++h)
               tma_load_3d(dst + h * kHalf, is_k ? &tm_kn : &tm_vn, bar(b_full), h * 64, w.g, w.q_first);
           }
+        } else if (MODE == MODE_VERIFY && t.s == w.b_count + 1) {
+          // the query-block keys of the unit's branches: 128 rows of k_new /
+          // v_new for kv head g from the first branch's first query token
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(b_full), 2 * kHalf);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(dst + h * kHalf, is_k ? &tm_kn : &tm_vn, bar(b_full), h * 64, w.g, w.tok_lo);
+          }
         } else {
           const int nblk = (min(kTileKeys, t.end - t.ks) + 15) >> 4;
           int32_t blk = 0;
           if (MODE == MODE_OWN) {
             if (lane < nblk)
               blk = p.table[static_cast<int64_t>(w.seq) * p.max_bps + w.n_shared + (t.ks >> 4) + lane];
+          } else if (MODE == MODE_VERIFY && t.s > 0) {
+            // an own tile of branch b_first + s - 1: its blocks after the shared ones
+            const DecBranch br = p.branches[w.b_first + t.s - 1];
+            if (lane < nblk) blk = p.table[static_cast<int64_t>(br.seq) * p.max_bps + br.n_shared + (t.ks >> 4) + lane];
           } else if (lane < nblk) {
             blk = ids[((t.ks - w.k_begin) >> 4) + lane];
           }
@@ -401,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (failed) break;
       }
-      if (!is_k && MODE == MODE_PREFIX) {
+      if (!is_k && (MODE == MODE_PREFIX || MODE == MODE_VERIFY)) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_IDS_FREE));
       }
@@ -513,6 +568,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         qpos = w.q_first + R / G;
         limit = valid ? p.q_plen[qpos] : 0;
       }
+      // fused verify: this row's branch, and bit c of qvis[c / 32] set when
+      // key c of the query-block tile (query token tok_lo + c) is the row's
+      // draft-tree ancestor or the row's own token
+      int32_t qbr = -1;
+      uint32_t qvis[4] = {0u, 0u, 0u, 0u};
+      if (MODE == MODE_VERIFY && valid) {
+        qbr = p.q_branch[qpos];
+        const DecBranch brq = p.branches[qbr];
+        const int qi = static_cast<int>(qpos) - brq.q_first;
+        uint32_t bits = p.tree_bits ? static_cast<uint32_t>(p.tree_bits[qpos]) : ((2u << qi) - 1u);
+        bits &= (1u << brq.q_len) - 1u;
+        const int rel = brq.q_first - w.tok_lo;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int sh = rel - 32 * k;
+          qvis[k] = sh >= 0 ? (sh < 32 ? bits << sh : 0u) : (sh > -32 ? bits >> -sh : 0u);
+        }
+      }
       float m_run = -INFINITY, l_run = 0.f;
       TileIter t;
       int j = 0;
@@ -547,10 +620,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t vis = klen;  // keys [0, vis) of the tile are visible
         if (MODE == MODE_FWD) {
           if (t.causal) vis = min(vis, limit - t.ks);
-        } else if (MODE == MODE_PREFIX) {
+        } else if (MODE == MODE_PREFIX || (MODE == MODE_VERIFY && t.s == 0)) {
           vis = min(vis, limit - t.ks);
+        } else if (MODE == MODE_VERIFY && t.s <= w.b_count) {
+          if (qbr != w.b_first + t.s - 1) vis = 0;  // another branch's own keys
         }
-        if (MODE == MODE_OWN && t.s == 1) {
+        if (MODE == MODE_VERIFY && t.s == w.b_count + 1) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (!((qvis[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
+        } else if (MODE == MODE_OWN && t.s == 1) {
           // query block: key c is query token c of this branch, visible iff it
           // is this token's draft-tree ancestor or the token itself
           const int qi = r / G;
@@ -720,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + kTmemO + lane_base + c * 32, v);
         tmem_wait_ld();
         if (valid) {
-          if (MODE == MODE_FWD) {
+          if (MODE == MODE_FWD || MODE == MODE_VERIFY) {
             uint4* dst = reinterpret_cast<uint4*>(p.o + (qpos * p.Hq + head) * kHeadDim + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -743,6 +822,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (valid) {
         if (MODE == MODE_FWD)
           p.lse[static_cast<int64_t>(head) * p.T + qpos] = lse_v;
+        else if (MODE == MODE_VERIFY)
+          p.lse[qpos * p.Hq + head] = lse_v;
         else
           p.part_lse[static_cast<int64_t>(w.row_base) + static_cast<int64_t>(w.g) * w.rows + r] = lse_v;
       }
@@ -773,7 +854,7 @@ int make_map(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, int rank, const
 template <int MODE>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mkn,
            const CUtensorMap& mvn, const Params& prm, cudaStream_t s, std::string* err) {
-  static bool attr_set[3] = {false, false, false};
+  static bool attr_set[4] = {false, false, false, false};
   if (!attr_set[MODE]) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) {
@@ -899,6 +980,50 @@ int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   p.branches = a.branches;
   p.tree_bits = a.tree_bits;
   return launch<MODE_OWN>(mq, mk, mv, mkn, mvn, p, s, err);
+}
+
+int launch_decode_verify_fused(const DecodeArgs& a, cudaStream_t s, std::string* err) {
+  if (a.n_items == 0) return PADOC_OK;
+  EncodeTiledFn enc = get_encode_fn(err);
+  if (!enc) return PADOC_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mkn, mvn;
+  // q viewed as [nq][Hkv][G][d]; box {64, G, 1, 128/G}
+  const cuuint64_t dq[4] = {128, static_cast<cuuint64_t>(a.group), static_cast<cuuint64_t>(a.Hkv),
+                            static_cast<cuuint64_t>(a.nq)};
+  const cuuint64_t sq[3] = {256, static_cast<cuuint64_t>(a.group) * 256, static_cast<cuuint64_t>(a.Hq) * 256};
+  const cuuint32_t bq[4] = {64, static_cast<cuuint32_t>(a.group), 1, static_cast<cuuint32_t>(kTileRows / a.group)};
+  const cuuint64_t dk[2] = {128, static_cast<cuuint64_t>(a.num_blocks) * a.Hkv * 16};
+  const cuuint64_t sk[1] = {256};
+  const cuuint32_t bk[2] = {64, 16};
+  // k_new / v_new viewed as [nq][Hkv][d]; box: 128 query tokens of one kv head
+  const cuuint64_t dn[3] = {128, static_cast<cuuint64_t>(a.Hkv), static_cast<cuuint64_t>(a.nq)};
+  const cuuint64_t sn[2] = {256, static_cast<cuuint64_t>(a.Hkv) * 256};
+  const cuuint32_t bn[3] = {64, 1, 128};
+  int rc = make_map(enc, &mq, a.q, 4, dq, sq, bq, err);
+  if (!rc) rc = make_map(enc, &mk, a.k_pool, 2, dk, sk, bk, err);
+  if (!rc) rc = make_map(enc, &mv, a.v_pool, 2, dk, sk, bk, err);
+  if (!rc) rc = make_map(enc, &mkn, a.k_new, 3, dn, sn, bn, err);
+  if (!rc) rc = make_map(enc, &mvn, a.v_new, 3, dn, sn, bn, err);
+  if (rc) return rc;
+  Params p{};
+  p.mode = MODE_VERIFY;
+  p.n_units = a.n_items * a.Hkv;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.group = a.group;
+  p.sl2 = a.scale * kLog2e;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.pages = a.pages;
+  p.items = a.items;
+  p.q_plen = a.q_plen;
+  p.table = a.table;
+  p.max_bps = a.max_bps;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.branches = a.branches;
+  p.tree_bits = a.tree_bits;
+  p.q_branch = a.q_branch;
+  return launch<MODE_VERIFY>(mq, mk, mv, mkn, mvn, p, s, err);
 }
 
 int read_and_clear_tc_error(cudaStream_t s, unsigned* word) {

@@ -989,9 +989,11 @@ struct DecodePlan {
   std::vector<DecItem> items;
   std::vector<DecBranch> branches;
   std::vector<int32_t> q_plen;
+  std::vector<int32_t> q_branch;  // branch of each query row
   int64_t part_rows = 0;
   bool tc_own = false;  // own pass on tensor cores (several query rows per branch and kv head)
-  size_t off_pages = 0, off_items = 0, off_branches = 0, off_qplen = 0, off_part_o = 0, off_part_lse = 0,
+  bool fused = false;   // verify: own suffix and query block walked by the prefix pass's units
+  size_t off_pages = 0, off_items = 0, off_branches = 0, off_qplen = 0, off_qbranch = 0, off_part_o = 0, off_part_lse = 0,
          total = 0;
 };
 
@@ -1019,7 +1021,20 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
     if (ql < 1 || ql > 16) return fail(PADOC_ERR_INVALID, "branch_decode: branch %d has %d query rows (1..16)", i, ql);
   }
   const int32_t nq = b->n_branches ? b->q_offsets[b->n_branches] : 0;
+  // One query token per branch gives G rows per (branch, kv head): the
+  // CUDA-core own pass streams that at HBM speed.  Draft-tree verify stacks
+  // up to 16 G rows, which needs the tensor cores.
+  pl->tc_own = b->n_branches > 0 && static_cast<int64_t>(nq) * G >= 4 * static_cast<int64_t>(b->n_branches);
+  // A verify step with G >= 2 fuses its own pass into the prefix pass when
+  // every page's prefix fits one chunk.  A row tile then spans at most 64
+  // query tokens, so the query blocks of the branches it touches (each at
+  // most 16 tokens) lie within 15 + 64 + 15 < 128 tokens: one key tile.
+  // PADOC_VERIFY_FUSED=0 keeps the two passes separate.
+  static const bool fuse_allowed = !(std::getenv("PADOC_VERIFY_FUSED") &&
+                                     std::string(std::getenv("PADOC_VERIFY_FUSED")) == "0");
+  bool want_fused = pl->tc_own && G >= 2 && fuse_allowed;
   pl->q_plen.assign(nq, 0);
+  pl->q_branch.assign(nq, 0);
   pl->branches.resize(b->n_branches);
   pl->pages.resize(b->n_pages);
   // chunk length from the total prefix work, so items fill the GPU
@@ -1053,6 +1068,14 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
   }
   int64_t ct = work_tiles / (2 * static_cast<int64_t>(n_sms));
   ct = std::max<int64_t>(8, std::min<int64_t>(kMaxChunkTiles, ct));
+  if (want_fused) {
+    int64_t max_tiles = 0;
+    for (int32_t p = 0; p < b->n_pages; ++p) max_tiles = std::max<int64_t>(max_tiles, (P[p] + kTileKeys - 1) / kTileKeys);
+    if (max_tiles <= kMaxChunkTiles)
+      ct = std::max(ct, max_tiles);  // one chunk per page
+    else
+      want_fused = false;
+  }
   int64_t rows = 0;
   for (int32_t p = 0; p < b->n_pages; ++p) {
     const int32_t b0 = b->branch_offsets[p], b1 = b->branch_offsets[p + 1];
@@ -1066,6 +1089,7 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
     pg.n_chunks = (tiles == 0 || pg.nq == 0) ? 0 : static_cast<int32_t>((tiles + ct - 1) / ct);
     pg.chunk_tokens = pg.n_chunks ? ((tiles + pg.n_chunks - 1) / pg.n_chunks) * kTileKeys : 0;
     pg.n_chunks = pg.chunk_tokens ? (pg.P + pg.chunk_tokens - 1) / pg.chunk_tokens : 0;
+    if (want_fused && pg.nq > 0 && pg.n_chunks == 0) pg.n_chunks = 1;  // no prefix: the unit walks own keys only
     pg.item_base = static_cast<int32_t>(pl->items.size());
     for (int32_t t = 0; t < pg.row_tiles && pg.n_chunks; ++t)
       for (int32_t c = 0; c < pg.n_chunks; ++c) {
@@ -1089,15 +1113,31 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
       br.q_first = b->q_offsets[i];
       br.q_len = b->q_offsets[i + 1] - b->q_offsets[i];
       br.q_in_page = br.q_first - pg.q_first;
-      for (int32_t r = br.q_first; r < br.q_first + br.q_len; ++r) pl->q_plen[r] = br.prefix_len;
+      for (int32_t r = br.q_first; r < br.q_first + br.q_len; ++r) {
+        pl->q_plen[r] = br.prefix_len;
+        pl->q_branch[r] = i;
+      }
+    }
+    if (want_fused) {
+      // the branches a row tile touches, and the first query token of the
+      // first of them (the fused unit's query-block tile starts there)
+      for (int32_t k = pg.item_base; k < static_cast<int32_t>(pl->items.size()); ++k) {
+        DecItem& it = pl->items[k];
+        const int32_t tok0 = pg.q_first + (it.tile * kTileRows) / G;
+        const int32_t tok1 = pg.q_first + (it.tile * kTileRows + it.rows - 1) / G;
+        const int32_t bf = pl->q_branch[tok0], bl = pl->q_branch[tok1];
+        it.b_first = bf;
+        it.b_count = bl - bf + 1;
+        it.tok_lo = pl->branches[bf].q_first;
+        if (pl->branches[bl].q_first + pl->branches[bl].q_len - it.tok_lo > kTileKeys)
+          return fail(PADOC_ERR_UNSUPPORTED, "branch_decode: query blocks of row tile %d span above %d tokens",
+                      it.tile, kTileKeys);
+      }
     }
   }
   if (rows >= (int64_t(1) << 31)) return fail(PADOC_ERR_UNSUPPORTED, "branch_decode: batch too large");
   pl->part_rows = rows;
-  // One query token per branch gives G rows per (branch, kv head): the
-  // CUDA-core own pass streams that at HBM speed.  Draft-tree verify stacks
-  // up to 16 G rows, which needs the tensor-core own pass.
-  pl->tc_own = b->n_branches > 0 && static_cast<int64_t>(nq) * G >= 4 * static_cast<int64_t>(b->n_branches);
+  pl->fused = want_fused;
   size_t off = 0;
   pl->off_pages = off;
   off = align_up(off + pl->pages.size() * sizeof(DecPage), 256);
@@ -1107,6 +1147,8 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
   off = align_up(off + pl->branches.size() * sizeof(DecBranch), 256);
   pl->off_qplen = off;
   off = align_up(off + pl->q_plen.size() * sizeof(int32_t), 256);
+  pl->off_qbranch = off;
+  off = align_up(off + pl->q_branch.size() * sizeof(int32_t), 256);
   pl->off_part_o = off;
   off = align_up(off + static_cast<size_t>(rows) * kHeadDim * sizeof(float), 256);
   pl->off_part_lse = off;
@@ -1155,6 +1197,7 @@ extern "C" int padoc_decode_plan_create(padoc_kv_pool* pool, const padoc_decode_
     std::memcpy(p->host.data() + p->pl.off_branches, p->pl.branches.data(),
                 p->pl.branches.size() * sizeof(DecBranch));
     std::memcpy(p->host.data() + p->pl.off_qplen, p->pl.q_plen.data(), p->pl.q_plen.size() * sizeof(int32_t));
+    std::memcpy(p->host.data() + p->pl.off_qbranch, p->pl.q_branch.data(), p->pl.q_branch.size() * sizeof(int32_t));
     res = p.release();
   });
   *out = res;
@@ -1206,6 +1249,7 @@ static DecodeArgs decode_args(const padoc_decode_plan* plan, const void* q, cons
   a.items = reinterpret_cast<const DecItem*>(w + pl.off_items);
   a.branches = reinterpret_cast<const DecBranch*>(w + pl.off_branches);
   a.q_plen = reinterpret_cast<const int32_t*>(w + pl.off_qplen);
+  a.q_branch = reinterpret_cast<const int32_t*>(w + pl.off_qbranch);
   a.table = pool->d_table;
   a.max_bps = pool->max_bps;
   a.n_pages = plan->n_pages;
@@ -1235,6 +1279,7 @@ extern "C" int padoc_decode_prefix_pass(const padoc_decode_plan* plan, const voi
                                         padoc_stream_t stream) {
   if (!plan) return fail(PADOC_ERR_INVALID, "decode_prefix_pass: null plan");
   if (plan->n_branches == 0 || plan->pl.items.empty()) return PADOC_OK;
+  if (plan->pl.fused) return PADOC_OK;  // the own pass walks the prefix too
   int rc = check_ws(plan, ws, SIZE_MAX);
   if (rc) return rc;
   if (!q || !aligned16(q)) return fail(PADOC_ERR_INVALID, "decode_prefix_pass: q must be a 16-byte aligned device pointer");
@@ -1266,7 +1311,9 @@ extern "C" int padoc_decode_own_pass(const padoc_decode_plan* plan, const void* 
   static const bool rows_major = std::getenv("PADOC_OWN_KERNEL") &&
                                  std::string(std::getenv("PADOC_OWN_KERNEL")) == "rows";
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (!plan->pl.tc_own)
+  if (plan->pl.fused)
+    rc = launch_decode_verify_fused(a, st, &err);
+  else if (!plan->pl.tc_own)
     rc = launch_decode_own(a, st, &err);
   else if (a.group <= 2 && !rows_major)
     rc = launch_decode_own_kmajor(a, st, &err);

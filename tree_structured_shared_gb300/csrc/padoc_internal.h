@@ -100,7 +100,9 @@ struct DecItem {
   int32_t page, tile, chunk;
   int32_t rows;      // valid rows of this row tile
   int32_t row_base;  // partial row index of head 0; head g adds g * rows
-  int32_t pad[3];
+  // fused verify: the branches whose query rows the tile holds, and the
+  // first query token of the first of them
+  int32_t b_first, b_count, tok_lo;
 };
 struct DecBranch {
   int32_t page, seq;
@@ -116,6 +118,7 @@ struct DecodeArgs {
   const DecItem* items;
   const DecBranch* branches;
   const int32_t* q_plen;  // [nq] prefix tokens visible to each query row
+  const int32_t* q_branch;  // [nq] branch of each query row
   const int32_t* table;   // device block table [max_seqs][max_bps]
   int32_t max_bps;
   int32_t n_pages, n_items, n_branches, nq;
@@ -142,6 +145,10 @@ int launch_decode_own(const DecodeArgs& a, cudaStream_t s, std::string* err);
 int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err);
 // Verify own pass with keys on the MMA's M side (Hq / Hkv of 1 or 2).
 int launch_decode_own_kmajor(const DecodeArgs& a, cudaStream_t s, std::string* err);
+// Verify step in one pass (plans marked fused): each (page, row tile, kv
+// head) walks the prefix, the own suffixes of the branches it holds and
+// their query block, and writes the final O and LSE.
+int launch_decode_verify_fused(const DecodeArgs& a, cudaStream_t s, std::string* err);
 int launch_kv_append(void* k_pool, void* v_pool, const int32_t* table_row, int32_t first_own,
                      int32_t n, int32_t Hkv, int32_t d, const void* k, const void* v,
                      cudaStream_t s, std::string* err);
