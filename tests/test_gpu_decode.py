@@ -81,6 +81,32 @@ def test_verify_prefix_above_one_chunk(harness):
     check(og, lg, O, L, "bf16", "verify, several prefix chunks per page")
 
 
+@pytest.mark.parametrize("verify", [True, False])
+def test_fragmented_pool(harness, verify):
+    """Pages and branches whose blocks are scattered over the pool in a
+    shuffled order: every key tile is loaded block by block (no tile of
+    eight consecutive blocks), for the fused verify pass and for the prefix
+    pass of branch decode."""
+    import torch
+    w = wl.small_decode(70 + verify, n_pages=3, max_prefix=1500, max_branches=5, max_own=400, verify=verify,
+                        Hq=4, Hkv=2)
+    vals = wl.decode_values(w, 70)
+    d = harness.Decode(w, vals, tree=verify, fragment=True)
+    def longest_run(b):
+        best = cur = 1
+        for i in range(1, len(b)):
+            cur = cur + 1 if b[i] == b[i - 1] + 1 else 1
+            best = max(best, cur)
+        return best
+    assert max(longest_run(d.pool.seq_blocks(s)) for s in d.page_seq + d.branch_seq) < 8
+    o, lse = d.run()
+    torch.cuda.synchronize()
+    padoc.device_status()
+    O, L = ta.branch_decode(w, vals, tree=verify)
+    check(o.float().cpu().numpy()[: w.n_queries], lse.cpu().numpy()[: w.n_queries], O, L, "bf16",
+          "fragmented pool")
+
+
 def _child_verify(tmp_path, env_over, seed=3):
     """One small draft-tree verify batch run in a child process under the
     given environment (the kernel choices are read once per process)."""

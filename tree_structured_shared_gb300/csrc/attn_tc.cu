@@ -298,7 +298,8 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kn,
-                   const __grid_constant__ CUtensorMap tm_vn, const Params p) {
+                   const __grid_constant__ CUtensorMap tm_vn, const __grid_constant__ CUtensorMap tm_k8,
+                   const __grid_constant__ CUtensorMap tm_v8, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base; offsetting the shared array itself keeps the
   // compiler aware that every pointer below is a shared-memory pointer
@@ -433,9 +434,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (lane < nblk) {
             blk = ids[((t.ks - w.k_begin) >> 4) + lane];
           }
+          // A tile of eight physically consecutive blocks comes in one box
+          // per half (the TMA unit takes some 75 cycles per 2 KB box, so
+          // sixteen boxes a tile for K and for V would bound the pass).
+          const int32_t b0 = __shfl_sync(0xffffffffu, blk, 0);
+          const bool run8 = nblk == 8 && __all_sync(0xffffffffu, lane >= 8 || blk == b0 + lane);
           if (lane == 0) mbar_arrive_expect_tx(bar(b_full), nblk * 2 * 2048);
           __syncwarp();
-          if (lane < nblk) {
+          if (run8) {
+            if (lane == 0)
+              for (int h = 0; h < 2; ++h) tma_load_4d(dst + h * kHalf, is_k ? &tm_k8 : &tm_v8, bar(b_full), h * 64, 0, w.g, b0);
+          } else if (lane < nblk) {
             const int32_t row = (blk * p.Hkv + w.g) * 16;
             for (int h = 0; h < 2; ++h) tma_load_2d(dst + h * kHalf + lane * 2048, tm, bar(b_full), h * 64, row);
           }
@@ -851,9 +860,21 @@ int make_map(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, int rank, const
   return PADOC_OK;
 }
 
+// The K / V pools viewed as [num_blocks][Hkv][16][d] with a box of eight
+// consecutive blocks of one kv head (16 KB, one half of a key tile).
+int make_pool8_maps(EncodeTiledFn enc, const DecodeArgs& a, CUtensorMap* mk8, CUtensorMap* mv8, std::string* err) {
+  const cuuint64_t d8[4] = {128, 16, static_cast<cuuint64_t>(a.Hkv), static_cast<cuuint64_t>(a.num_blocks)};
+  const cuuint64_t s8[3] = {256, 4096, static_cast<cuuint64_t>(a.Hkv) * 4096};
+  const cuuint32_t b8[4] = {64, 16, 1, 8};
+  int rc = make_map(enc, mk8, a.k_pool, 4, d8, s8, b8, err);
+  if (!rc) rc = make_map(enc, mv8, a.v_pool, 4, d8, s8, b8, err);
+  return rc;
+}
+
 template <int MODE>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mkn,
-           const CUtensorMap& mvn, const Params& prm, cudaStream_t s, std::string* err) {
+           const CUtensorMap& mvn, const CUtensorMap& mk8, const CUtensorMap& mv8, const Params& prm, cudaStream_t s,
+           std::string* err) {
   static bool attr_set[4] = {false, false, false, false};
   if (!attr_set[MODE]) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -864,7 +885,7 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
     attr_set[MODE] = true;
   }
   const int grid = std::min(prm.n_units, num_sms());
-  attn_tc_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mkn, mvn, prm);
+  attn_tc_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mkn, mvn, mk8, mv8, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *err = std::string("attention kernel launch: ") + cudaGetErrorString(e);
@@ -901,7 +922,7 @@ int launch_fwd_bf16(const FwdArgs& a, cudaStream_t s, std::string* err) {
   p.T = a.T;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
-  return launch<MODE_FWD>(mq, mk, mv, mk, mv, p, s, err);
+  return launch<MODE_FWD>(mq, mk, mv, mk, mv, mk, mv, p, s, err);
 }
 
 int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err) {
@@ -936,7 +957,10 @@ int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
-  return launch<MODE_PREFIX>(mq, mk, mv, mk, mv, p, s, err);
+  CUtensorMap mk8, mv8;
+  rc = make_pool8_maps(enc, a, &mk8, &mv8, err);
+  if (rc) return rc;
+  return launch<MODE_PREFIX>(mq, mk, mv, mk, mv, mk8, mv8, p, s, err);
 }
 
 int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err) {
@@ -979,7 +1003,10 @@ int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   p.part_lse = a.part_lse;
   p.branches = a.branches;
   p.tree_bits = a.tree_bits;
-  return launch<MODE_OWN>(mq, mk, mv, mkn, mvn, p, s, err);
+  CUtensorMap mk8, mv8;
+  rc = make_pool8_maps(enc, a, &mk8, &mv8, err);
+  if (rc) return rc;
+  return launch<MODE_OWN>(mq, mk, mv, mkn, mvn, mk8, mv8, p, s, err);
 }
 
 int launch_decode_verify_fused(const DecodeArgs& a, cudaStream_t s, std::string* err) {
@@ -1023,7 +1050,10 @@ int launch_decode_verify_fused(const DecodeArgs& a, cudaStream_t s, std::string*
   p.branches = a.branches;
   p.tree_bits = a.tree_bits;
   p.q_branch = a.q_branch;
-  return launch<MODE_VERIFY>(mq, mk, mv, mkn, mvn, p, s, err);
+  CUtensorMap mk8, mv8;
+  rc = make_pool8_maps(enc, a, &mk8, &mv8, err);
+  if (rc) return rc;
+  return launch<MODE_VERIFY>(mq, mk, mv, mkn, mvn, mk8, mv8, p, s, err);
 }
 
 int read_and_clear_tc_error(cudaStream_t s, unsigned* word) {

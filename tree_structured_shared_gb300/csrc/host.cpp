@@ -563,7 +563,11 @@ struct padoc_kv_pool {
   void* v = nullptr;
   int32_t nb = 0, bs = 16, Hkv = 0, d = 0, dtype = 0, max_seqs = 0, max_bps = 0;
   std::vector<int32_t> refcnt;
-  std::vector<int32_t> free_blocks;  // stack
+  // Free blocks as a stack, lowest id on top at creation.  Blocks go back
+  // last first, so a freed run comes out again in ascending order: the
+  // decode kernels load 8 physically consecutive blocks of a key tile with
+  // one copy.
+  std::vector<int32_t> free_blocks;
   std::vector<Seq> seqs;
   std::vector<int32_t> free_seqs;    // stack
   int64_t fault_after = -1;          // fail the allocation that would exceed this count
@@ -750,7 +754,7 @@ extern "C" int padoc_kv_trim(padoc_kv_pool* pool, int32_t seq) {
   Seq& s = pool->seqs[seq];
   const size_t keep = static_cast<size_t>(s.n_shared) + (s.len - s.fork_len + pool->bs - 1) / pool->bs;
   if (s.blocks.size() > keep) {
-    for (size_t i = keep; i < s.blocks.size(); ++i) pool->drop_block(s.blocks[i]);
+    for (size_t i = s.blocks.size(); i-- > keep;) pool->drop_block(s.blocks[i]);
     s.blocks.resize(keep);
     pool->mark(seq);
   }
@@ -761,7 +765,7 @@ extern "C" int padoc_kv_release(padoc_kv_pool* pool, int32_t seq) {
   if (!pool) return fail(PADOC_ERR_INVALID, "kv_release: null pool");
   if (!pool->seq_ok(seq)) return fail(PADOC_ERR_INVALID, "kv_release: %d is not a live sequence", seq);
   Seq& s = pool->seqs[seq];
-  for (int32_t b : s.blocks) pool->drop_block(b);
+  for (size_t i = s.blocks.size(); i-- > 0;) pool->drop_block(s.blocks[i]);
   s = Seq();
   pool->mark(seq);
   pool->free_seqs.push_back(seq);

@@ -156,17 +156,27 @@ class Decode:
     block, all resident on the GPU."""
 
     def __init__(self, w: wl.DecodeWorkload, vals: Optional[wl.DecodeValues] = None, seed: int = 0,
-                 device="cuda", tree: bool = True, slack_blocks: int = 8):
+                 device="cuda", tree: bool = True, slack_blocks: int = 8, fragment: bool = False):
+        """fragment: the pool has twice the blocks, every other one held by a
+        spacer sequence and the rest handed out in a shuffled order, so no
+        two blocks of a sequence are physically consecutive by design."""
         self.w = w
         Hkv, d = w.Hkv, w.d
         nb = sum((p.prefix_len + 15) // 16 for p in w.pages)
         nb += sum((L + 15) // 16 for p in w.pages for L in p.own_len) + slack_blocks
+        n_spacers = nb if fragment else 0
+        nb += n_spacers
         max_bps = max([(p.prefix_len + 15) // 16 + (max(p.own_len or [0]) + 15) // 16 + 2 for p in w.pages] + [4])
         self.k_pool = torch.empty(nb, Hkv, 16, d, dtype=torch.bfloat16, device=device)
         self.v_pool = torch.empty(nb, Hkv, 16, d, dtype=torch.bfloat16, device=device)
         self.pool = padoc.KVPool(self.k_pool, self.v_pool, nb, Hkv, d,
-                                 max_seqs=len(w.pages) + w.n_branches + 8, max_blocks_per_seq=max_bps)
+                                 max_seqs=len(w.pages) + w.n_branches + 8 + (nb if fragment else 0),
+                                 max_blocks_per_seq=max_bps)
         self.pool.sync()
+        if fragment:
+            spacers = [self.pool.alloc(16) for _ in range(nb)]
+            for i in np.random.default_rng(seed + 7919).permutation(nb)[:n_spacers]:
+                self.pool.release(spacers[i])
         self.gen = DeviceDecodeValues(w, seed, device) if vals is None else None
         page_seq, branch_seq, boff, qoff = [], [], [0], [0]
         b = 0
