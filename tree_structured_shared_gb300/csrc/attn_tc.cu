@@ -634,6 +634,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (MODE == MODE_VERIFY && t.s <= w.b_count) {
           if (qbr != w.b_first + t.s - 1) vis = 0;  // another branch's own keys
         }
+        // A row that sees no key of the tile takes P = 0 through an infinite
+        // exponent offset; it still masks keys past the tile's end (stale or
+        // unwritten bytes), but needs no per-key mask below that.
+        const bool row_dead = vis <= 0 && !((MODE == MODE_VERIFY && t.s == w.b_count + 1) || (MODE == MODE_OWN && t.s == 1));
+        if (row_dead) vis = klen;
         if (MODE == MODE_VERIFY && t.s == w.b_count + 1) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -665,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[120 + i]);
           tmax = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+          if (row_dead) tmax = -INFINITY;
         }
         const float mt = tmax * p.sl2;
         const bool grow = mt > m_run + kRescaleThreshold;
@@ -673,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= alpha;
           m_run = mt;
         }
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        const float m_use = row_dead ? INFINITY : ((m_run == -INFINITY) ? 0.f : m_run);
         {
           // x = s * sl2 - m two lanes per instruction; the same partial sums
           // (lane k of the row sum takes columns c with c % 8 == k)
