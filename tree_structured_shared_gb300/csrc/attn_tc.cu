@@ -143,6 +143,7 @@ struct Unit {
   int32_t page, tile, rows, row_base, k_begin, k_end, seq, q_first;
   // own
   int32_t own_len, n_shared, q_len, q_in_page;
+  int32_t n_tiles;  // key tiles of the unit
   // fused verify
   int32_t b_first, b_count, tok_lo;
 };
@@ -164,6 +165,7 @@ __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
     w.kv_first = qs.kv_first;
     w.kv_count = qs.kv_count;
     w.tile_last = min(it.tile_start + p.plan.tile_tokens, w.q_end) - 1;
+    w.n_tiles = it.n_tiles;
   } else if (p.mode == MODE_OWN) {
     const DecBranch br = p.branches[item];
     w.page = br.page;
@@ -174,6 +176,7 @@ __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
     w.q_len = br.q_len;
     w.q_in_page = br.q_in_page;
     w.rows = br.q_len * p.group;
+    w.n_tiles = (br.own_len + kTileKeys - 1) / kTileKeys + 1;  // own suffix, then the query block
   } else {
     const DecItem it = p.items[item];
     const DecPage pg = p.pages[it.page];
@@ -188,18 +191,25 @@ __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
     w.b_first = it.b_first;
     w.b_count = it.b_count;
     w.tok_lo = it.tok_lo;
+    w.n_tiles = it.n_tiles;
   }
   return w;
 }
 
 // Key tiles of a unit are enumerated in one fixed order by every role.
+// Walk over a unit's key tiles.  The descriptor of the segment after the
+// current one (forward: its KV segment; fused verify: the next own suffix's
+// length) is loaded on entering a segment, so the switch does not wait on
+// global memory.
 struct TileIter {
   int32_t s, s_end, ks, end, causal;
+  KVSeg nx;
 };
 
 __device__ __forceinline__ bool seg_setup(const Params& p, const Unit& w, TileIter& t) {
   while (t.s < t.s_end) {
-    const KVSeg kv = p.plan.kvsegs[t.s];
+    const KVSeg kv = t.nx;
+    if (t.s + 1 < t.s_end) t.nx = p.plan.kvsegs[t.s + 1];
     int32_t end = kv.start + kv.len;
     if (kv.causal) end = min(end, w.tile_last + 1);
     if (end > kv.start) {
@@ -214,7 +224,8 @@ __device__ __forceinline__ bool seg_setup(const Params& p, const Unit& w, TileIt
 }
 
 // Fused verify: segment 0 is the prefix chunk, segments 1 .. b_count the own
-// suffixes of the unit's branches, segment b_count + 1 the query-block tile.
+// suffixes of the unit's branches (t.nx.len: the length of segment s + 1 when
+// it is one), segment b_count + 1 the query-block tile.
 __device__ __forceinline__ bool verify_setup(const Params& p, const Unit& w, TileIter& t) {
   while (t.s < t.s_end) {
     t.ks = 0;
@@ -222,10 +233,11 @@ __device__ __forceinline__ bool verify_setup(const Params& p, const Unit& w, Til
       t.ks = w.k_begin;
       t.end = w.k_end;
     } else if (t.s <= w.b_count) {
-      t.end = p.branches[w.b_first + t.s - 1].own_len;
+      t.end = t.nx.len;
     } else {
       t.end = 1;
     }
+    if (t.s + 1 <= w.b_count) t.nx.len = p.branches[w.b_first + t.s].own_len;
     if (t.ks < t.end) return true;
     ++t.s;
   }
@@ -242,6 +254,7 @@ __device__ __forceinline__ bool tiles_begin(const Params& p, const Unit& w, Tile
   if (p.mode == MODE_FWD) {
     t.s = w.kv_first;
     t.s_end = w.kv_first + w.kv_count;
+    if (t.s < t.s_end) t.nx = p.plan.kvsegs[t.s];
     return seg_setup(p, w, t);
   }
   if (p.mode == MODE_OWN) {
@@ -282,12 +295,9 @@ __device__ __forceinline__ bool tiles_next(const Params& p, const Unit& w, TileI
   return false;
 }
 
-__device__ __forceinline__ int count_tiles(const Params& p, const Unit& w) {
-  int n = 0;
-  TileIter t;
-  for (bool ok = tiles_begin(p, w, t); ok; ok = tiles_next(p, w, t)) ++n;
-  return n;
-}
+// Key tiles of the unit, counted by the host plan (the walk itself reads a
+// segment list from global memory, a chain of loads every role would wait on).
+__device__ __forceinline__ int count_tiles(const Params&, const Unit& w) { return w.n_tiles; }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned site) {
   *abort = 1;

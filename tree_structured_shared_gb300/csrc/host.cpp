@@ -349,7 +349,7 @@ static std::vector<FwdItem> build_items(const padoc_tree_desc* desc, int tile_to
         if (kv.causal) len = std::min<int64_t>(kv.len, t1 - kv.start);
         c += (len + kTileKeys - 1) / kTileKeys;
       }
-      v.push_back({c, {static_cast<int32_t>(s), t0}});
+      v.push_back({c, {static_cast<int32_t>(s), t0, static_cast<int32_t>(c), 0}});
     }
   }
   std::stable_sort(v.begin(), v.end(), [](const Cost& a, const Cost& b) { return a.cost > b.cost; });
@@ -1103,6 +1103,8 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
         it.chunk = c;
         it.rows = std::min(kTileRows, pg.nq * G - t * kTileRows);
         it.row_base = static_cast<int32_t>(rows);
+        const int32_t k0 = c * pg.chunk_tokens, k1 = std::min(pg.P, k0 + pg.chunk_tokens);
+        it.n_tiles = k1 > k0 ? (k1 - k0 + kTileKeys - 1) / kTileKeys : 0;
         rows += static_cast<int64_t>(it.rows) * pool->Hkv;
         pl->items.push_back(it);
       }
@@ -1133,6 +1135,8 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
         it.b_first = bf;
         it.b_count = bl - bf + 1;
         it.tok_lo = pl->branches[bf].q_first;
+        for (int32_t b = bf; b <= bl; ++b) it.n_tiles += (pl->branches[b].own_len + kTileKeys - 1) / kTileKeys;
+        it.n_tiles += 1;  // the query-block tile
         if (pl->branches[bl].q_first + pl->branches[bl].q_len - it.tok_lo > kTileKeys)
           return fail(PADOC_ERR_UNSUPPORTED, "branch_decode: query blocks of row tile %d span above %d tokens",
                       it.tile, kTileKeys);

@@ -21,6 +21,8 @@ struct KVSeg {
 // One query tile: tile_tokens consecutive tokens of one query segment.
 struct FwdItem {
   int32_t qseg, tile_start;
+  int32_t n_tiles;  // key tiles the tile's walk visits (every kernel role counts on it)
+  int32_t pad;
 };
 
 constexpr int kTileKeys = 128;  // keys per K/V tile
@@ -103,6 +105,8 @@ struct DecItem {
   // fused verify: the branches whose query rows the tile holds, and the
   // first query token of the first of them
   int32_t b_first, b_count, tok_lo;
+  int32_t n_tiles;  // key tiles of the unit (prefix chunk; fused verify: + own suffixes + query block)
+  int32_t pad[3];
 };
 struct DecBranch {
   int32_t page, seq;
