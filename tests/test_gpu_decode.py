@@ -107,6 +107,24 @@ def test_fragmented_pool(harness, verify):
           "fragmented pool")
 
 
+def test_verify_output_16_byte_aligned(harness):
+    """The fused verify pass writing O into a tensor that is 16- but not
+    32-byte aligned (16-byte stores per row)."""
+    import torch
+    w = wl.small_decode(80, n_pages=3, max_prefix=700, max_branches=6, max_own=300, Hq=4, Hkv=2)
+    vals = wl.decode_values(w, 80)
+    d = harness.Decode(w, vals, tree=True)
+    buf = torch.empty(d.o.numel() + 8, dtype=d.o.dtype, device=d.o.device)
+    d.o = buf[8:].view(d.o.shape)
+    assert d.o.data_ptr() % 32 == 16
+    o, lse = d.run()
+    torch.cuda.synchronize()
+    padoc.device_status()
+    O, L = ta.branch_decode(w, vals, tree=True)
+    check(o.float().cpu().numpy()[: w.n_queries], lse.cpu().numpy()[: w.n_queries], O, L, "bf16",
+          "verify, 16-byte aligned output")
+
+
 def _child_verify(tmp_path, env_over, seed=3):
     """One small draft-tree verify batch run in a child process under the
     given environment (the kernel choices are read once per process)."""

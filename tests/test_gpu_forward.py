@@ -128,3 +128,23 @@ def test_repeat_runs_bit_identical(harness):
         torch.cuda.synchronize()
         assert torch.equal(o, o0) and torch.equal(l, l0)
     padoc.device_status()
+
+
+def test_output_16_byte_aligned(harness):
+    """An output tensor that is 16- but not 32-byte aligned (the ABI's
+    promise): the epilogue stores each row in 16-byte pieces instead of
+    32-byte ones.  Random bf16 pages against the oracle."""
+    import torch
+    w = wl.random_pages(31, n_pages=2, max_prefix=300, max_regions=5, max_layout=20, max_content=150,
+                        Hq=4, Hkv=2, d=128, dtype="bf16")
+    q, k, v = wl.tree_qkv(w, 31)
+    f = harness.Forward(w, q, k, v)
+    buf = torch.empty(f.o.numel() + 8, dtype=f.o.dtype, device=f.o.device)
+    f.o = buf[8:].view(f.o.shape)
+    assert f.o.data_ptr() % 32 == 16
+    o, lse = f.run()
+    torch.cuda.synchronize()
+    padoc.device_status()
+    O, L = ta.tree_forward(q, k, v, w.pages)
+    check(o.float().cpu().numpy()[: w.n_tokens], lse.cpu().numpy()[:, : w.n_tokens], O, L, "bf16",
+          "16-byte aligned output")

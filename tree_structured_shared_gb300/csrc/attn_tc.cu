@@ -118,6 +118,7 @@ struct Params {
   FwdPlan plan;
   int64_t T;
   __nv_bfloat16* o;
+  int o_v8;  // o is 32-byte aligned (rows then take 32-byte stores)
   float* lse;
   // prefix pass
   const DecPage* pages;
@@ -818,27 +819,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+      {
+        // all of O's row in flight before one wait, then 32-byte stores
+        uint32_t v[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + kTmemO + lane_base + c * 32, v);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + kTmemO + lane_base + c * 32, v[c]);
         tmem_wait_ld();
         if (valid) {
           if (MODE == MODE_FWD || MODE == MODE_VERIFY) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + (qpos * p.Hq + head) * kHeadDim + c * 32);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(p.o + (qpos * p.Hq + head) * kHeadDim);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * inv_l, __uint_as_float(v[8 * i + 1]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv_l, __uint_as_float(v[8 * i + 3]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv_l, __uint_as_float(v[8 * i + 5]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv_l, __uint_as_float(v[8 * i + 7]) * inv_l));
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  pk[i] = pack_bf16x2(__uint_as_float(v[c][16 * h + 2 * i]) * inv_l,
+                                      __uint_as_float(v[c][16 * h + 2 * i + 1]) * inv_l);
+                if (p.o_v8) {
+                  st_global_v8(dst + c * 16 + h * 8, pk);
+                } else {
+                  uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16 + h * 8);
+                  d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                  d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+              }
           } else {
-            float4* dst = reinterpret_cast<float4*>(
-                p.part_o + (static_cast<int64_t>(w.row_base) + static_cast<int64_t>(w.g) * w.rows + r) * kHeadDim + c * 32);
+            float* dst = p.part_o + (static_cast<int64_t>(w.row_base) + static_cast<int64_t>(w.g) * w.rows + r) * kHeadDim;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i + 0]) * inv_l, __uint_as_float(v[4 * i + 1]) * inv_l,
-                                   __uint_as_float(v[4 * i + 2]) * inv_l, __uint_as_float(v[4 * i + 3]) * inv_l);
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                uint32_t x[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = __float_as_uint(__uint_as_float(v[c][8 * h + i]) * inv_l);
+                st_global_v8(dst + c * 32 + h * 8, x);
+              }
           }
         }
       }
@@ -937,6 +954,7 @@ int launch_fwd_bf16(const FwdArgs& a, cudaStream_t s, std::string* err) {
   p.plan = a.plan;
   p.T = a.T;
   p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.o_v8 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
   p.lse = a.lse;
   return launch<MODE_FWD>(mq, mk, mv, mk, mv, mk, mv, p, s, err);
 }
@@ -1009,6 +1027,7 @@ int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   p.group = a.group;
   p.sl2 = a.scale * kLog2e;
   p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.o_v8 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
   p.lse = a.lse;
   p.pages = a.pages;
   p.items = a.items;
@@ -1056,6 +1075,7 @@ int launch_decode_verify_fused(const DecodeArgs& a, cudaStream_t s, std::string*
   p.group = a.group;
   p.sl2 = a.scale * kLog2e;
   p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.o_v8 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
   p.lse = a.lse;
   p.pages = a.pages;
   p.items = a.items;
