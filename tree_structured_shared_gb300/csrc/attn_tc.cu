@@ -91,7 +91,9 @@ enum {
   B_O_DONE = 9,      // +buffer (3): P V of tile k (V stage k % 3) has run
   B_IDS_READY = 12,  // prefix pass: the chunk's block ids are staged
   B_IDS_FREE = 13,   // prefix pass: the V producer is done with them
-  N_BARS = 14
+  B_UNIT_FULL = 14,  // +slot (4), decode: the unit ring's slot holds the next unit
+  B_UNIT_EMPTY = 18, // +slot (4), count 6: the MMA thread, the V producer and the softmax warps read it
+  N_BARS = 22
 };
 // Tiles are numbered k across all units of the CTA.  Tile k uses K stage, S
 // buffer and V stage k % 3 alike, so the S_FULL commit also frees its K stage
@@ -103,6 +105,13 @@ enum {
 // commits twice.
 static_assert(kStages == kSBufs, "K / V stages must match the S buffers");
 static_assert(N_BARS * 8 + 8 <= SM_IDS - SM_BAR, "barrier area");
+// Decode kernels take their units from a counter in the workspace, in order
+// (so the CTAs at work at one time still share pages), as they free up: the
+// K producer draws two units ahead and publishes them in a ring of kURing
+// slots after the barriers; the other roles read them there.
+constexpr int kURing = 4;
+constexpr int SM_URING = SM_BAR + 192;
+static_assert(N_BARS * 8 + 8 <= 192 && SM_URING + kURing * 4 <= SM_IDS, "unit ring");
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kTmemO = 384;           // TMEM columns [384, 512): O (f32)
@@ -129,6 +138,7 @@ struct Params {
   const __nv_bfloat16* q;
   float* part_o;
   float* part_lse;
+  int32_t* work;  // decode: unit counter, zero at launch
   // own pass
   const DecBranch* branches;
   const uint16_t* tree_bits;
@@ -300,6 +310,26 @@ __device__ __forceinline__ bool tiles_next(const Params& p, const Unit& w, TileI
 // segment list from global memory, a chain of loads every role would wait on).
 __device__ __forceinline__ int count_tiles(const Params&, const Unit& w) { return w.n_tiles; }
 
+// The next unit of a role that reads the unit ring (decode), or of the
+// static round robin (forward).  `k` counts the units the role has taken;
+// `single` when one thread runs the role.  False when a wait gave up.
+template <int MODE>
+__device__ __forceinline__ bool take_unit(const Params& p, uint32_t& k, int& u, volatile int32_t* uring,
+                                          uint64_t* bars, volatile int* abort, bool single) {
+  if (MODE == MODE_FWD) {
+    u = blockIdx.x + static_cast<int>(k++) * gridDim.x;
+    return true;
+  }
+  const int slot = k % kURing;
+  const bool ok = mbar_wait(smem_u32(&bars[B_UNIT_FULL + slot]), (k / kURing) & 1, abort);
+  if (single ? !ok : !__all_sync(0xffffffffu, ok)) return false;
+  u = uring[slot];
+  if (!single) __syncwarp();
+  if (single || (threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars[B_UNIT_EMPTY + slot]));
+  ++k;
+  return true;
+}
+
 __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned site) {
   *abort = 1;
   atomicOr(&g_tc_err, site);
@@ -319,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_BAR + N_BARS * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + SM_BAR + N_BARS * 8 + 4);
+  volatile int32_t* uring = reinterpret_cast<volatile int32_t*>(smem + SM_URING);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
@@ -327,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t cnt = 1;
       if (i >= B_P_FULL && i < B_P_FULL + kSBufs) cnt = 6;
+      if (i >= B_UNIT_EMPTY && i < B_UNIT_EMPTY + kURing) cnt = 6;
       if (i == B_QK0_FULL) cnt = 2;
       mbar_init(bar(i), cnt);
     }
@@ -366,9 +398,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* ids = reinterpret_cast<int32_t*>(smem + SM_IDS);
     uint32_t it = 0, item_it = 0;
     bool failed = false;
-    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+    // decode, K producer: draw a unit from the counter and publish it in
+    // the ring (-1 when a wait gave up).  The next unit is drawn once the
+    // current one's K tiles are issued: late enough that no CTA takes work
+    // early, early enough that the draw overlaps the wait for Q.
+    uint32_t n_pub = 0;
+    auto publish = [&]() -> int {
+      const int slot = n_pub % kURing;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_UNIT_EMPTY + slot), ((n_pub / kURing) & 1) ^ 1, abort)))
+        return -1;
+      int v = 0;
+      if (lane == 0) {
+        v = atomicAdd(p.work, 1);
+        uring[slot] = v;
+        mbar_arrive(bar(B_UNIT_FULL + slot));
+      }
+      ++n_pub;
+      return __shfl_sync(0xffffffffu, v, 0);
+    };
+    int q_next = 0;  // K producer: the unit published, not yet loaded
+    if (MODE != MODE_FWD && is_k) {
+      q_next = publish();
+      if (q_next < 0) failed = true;
+    }
+    auto publish_next = [&]() -> bool {
+      if (MODE == MODE_FWD || !is_k) return true;
+      q_next = publish();
+      return q_next >= 0;
+    };
+    uint32_t n_taken = 0;
+    while (!failed) {
+      int u;
+      if (MODE == MODE_FWD || !is_k) {
+        if (!take_unit<MODE>(p, n_taken, u, uring, bars, abort, false)) {
+          failed = true;
+          break;
+        }
+      } else {
+        u = q_next;
+      }
+      if (u >= p.n_units) break;
       const Unit w = load_unit(p, u);
-      if (count_tiles(p, w) == 0) continue;
+      if (count_tiles(p, w) == 0) {
+        if (!publish_next()) {
+          failed = true;
+          break;
+        }
+        continue;
+      }
       if (is_k) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (item_it & 1) ^ 1, abort))) { failed = true; break; }
         if (lane == 0) {
@@ -462,6 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (failed) break;
+      if (!publish_next()) {
+        failed = true;
+        break;
+      }
       if (is_k) {
         // tiles whose K tile two further on does not exist (the unit's last
         // two) still get the K producer's arrival on P_FULL.  Arriving for
@@ -515,7 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_ph ^= 1;
         }
       };
-      for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+      uint32_t n_taken = 0;
+      while (!failed) {
+        int u;
+        if (!take_unit<MODE>(p, n_taken, u, uring, bars, abort, true)) {
+          failed = true;
+          break;
+        }
+        if (u >= p.n_units) break;
         const Unit w = load_unit(p, u);
         const int n = count_tiles(p, w);
         if (n == 0) continue;
@@ -561,7 +649,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t s_it = 0, p_it = 0, pv_base = 0;
     bool failed = false;
-    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+    uint32_t n_taken = 0;
+    while (!failed) {
+      int u;
+      if (!take_unit<MODE>(p, n_taken, u, uring, bars, abort, false)) {
+        failed = true;
+        break;
+      }
+      if (u >= p.n_units) break;
       const Unit w = load_unit(p, u);
       const int n = count_tiles(p, w);
       if (n == 0) continue;
@@ -994,6 +1089,15 @@ int launch_decode_prefix(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   CUtensorMap mk8, mv8;
   rc = make_pool8_maps(enc, a, &mk8, &mv8, err);
   if (rc) return rc;
+  p.work = a.work;
+  {
+    // units are drawn from this counter in order
+    const cudaError_t e = cudaMemsetAsync(a.work, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) {
+      *err = std::string("cudaMemsetAsync of the unit counter: ") + cudaGetErrorString(e);
+      return PADOC_ERR_CUDA;
+    }
+  }
   return launch<MODE_PREFIX>(mq, mk, mv, mk, mv, mk8, mv8, p, s, err);
 }
 
@@ -1041,6 +1145,15 @@ int launch_decode_own_tc(const DecodeArgs& a, cudaStream_t s, std::string* err) 
   CUtensorMap mk8, mv8;
   rc = make_pool8_maps(enc, a, &mk8, &mv8, err);
   if (rc) return rc;
+  p.work = a.work;
+  {
+    // units are drawn from this counter in order
+    const cudaError_t e = cudaMemsetAsync(a.work, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) {
+      *err = std::string("cudaMemsetAsync of the unit counter: ") + cudaGetErrorString(e);
+      return PADOC_ERR_CUDA;
+    }
+  }
   return launch<MODE_OWN>(mq, mk, mv, mkn, mvn, mk8, mv8, p, s, err);
 }
 
@@ -1089,6 +1202,15 @@ int launch_decode_verify_fused(const DecodeArgs& a, cudaStream_t s, std::string*
   CUtensorMap mk8, mv8;
   rc = make_pool8_maps(enc, a, &mk8, &mv8, err);
   if (rc) return rc;
+  p.work = a.work;
+  {
+    // units are drawn from this counter in order
+    const cudaError_t e = cudaMemsetAsync(a.work, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) {
+      *err = std::string("cudaMemsetAsync of the unit counter: ") + cudaGetErrorString(e);
+      return PADOC_ERR_CUDA;
+    }
+  }
   return launch<MODE_VERIFY>(mq, mk, mv, mkn, mvn, mk8, mv8, p, s, err);
 }
 

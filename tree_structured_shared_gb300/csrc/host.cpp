@@ -998,7 +998,7 @@ struct DecodePlan {
   bool tc_own = false;  // own pass on tensor cores (several query rows per branch and kv head)
   bool fused = false;   // verify: own suffix and query block walked by the prefix pass's units
   size_t off_pages = 0, off_items = 0, off_branches = 0, off_qplen = 0, off_qbranch = 0, off_part_o = 0, off_part_lse = 0,
-         total = 0;
+         off_work = 0, total = 0;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1161,6 +1161,8 @@ int plan_decode(const padoc_kv_pool* pool, const padoc_decode_batch* b, int32_t 
   off = align_up(off + static_cast<size_t>(rows) * kHeadDim * sizeof(float), 256);
   pl->off_part_lse = off;
   off = align_up(off + static_cast<size_t>(rows) * sizeof(float), 256);
+  pl->off_work = off;  // the unit counter of the tensor-core passes
+  off = align_up(off + sizeof(int32_t), 256);
   pl->total = off;
   return PADOC_OK;
 }
@@ -1277,6 +1279,7 @@ static DecodeArgs decode_args(const padoc_decode_plan* plan, const void* q, cons
   a.lse = lse;
   a.part_o = reinterpret_cast<float*>(w + pl.off_part_o);
   a.part_lse = reinterpret_cast<float*>(w + pl.off_part_lse);
+  a.work = reinterpret_cast<int32_t*>(w + pl.off_work);
   a.k_pool = pool->k;
   a.v_pool = pool->v;
   a.num_blocks = pool->nb;

@@ -136,6 +136,7 @@ struct DecodeArgs {
   float* lse;
   float* part_o;    // [rows][d] f32 normalised partial outputs of the prefix pass
   float* part_lse;  // [rows] f32
+  int32_t* work;    // unit counter of the tensor-core passes (zeroed by their launchers)
   const void* k_pool;
   const void* v_pool;
   int64_t num_blocks;
