@@ -155,6 +155,7 @@ struct Unit {
   // own
   int32_t own_len, n_shared, q_len, q_in_page;
   int32_t n_tiles;  // key tiles of the unit
+  KVSeg kv0;        // forward: the first key segment
   // fused verify
   int32_t b_first, b_count, tok_lo;
 };
@@ -170,13 +171,13 @@ __device__ __forceinline__ Unit load_unit(const Params& p, int u) {
   const int item = p.mode == MODE_OWN ? u / p.Hkv : u % n_it;
   if (p.mode == MODE_FWD) {
     const FwdItem it = p.plan.items[item];
-    const QSeg qs = p.plan.qsegs[it.qseg];
     w.tile_start = it.tile_start;
-    w.q_end = qs.q_start + qs.q_len;
-    w.kv_first = qs.kv_first;
-    w.kv_count = qs.kv_count;
-    w.tile_last = min(it.tile_start + p.plan.tile_tokens, w.q_end) - 1;
+    w.q_end = it.q_end;
+    w.kv_first = it.kv_first;
+    w.kv_count = it.kv_count;
+    w.tile_last = it.tile_last;
     w.n_tiles = it.n_tiles;
+    w.kv0 = it.kv0;
   } else if (p.mode == MODE_OWN) {
     const DecBranch br = p.branches[item];
     w.page = br.page;
@@ -265,7 +266,7 @@ __device__ __forceinline__ bool tiles_begin(const Params& p, const Unit& w, Tile
   if (p.mode == MODE_FWD) {
     t.s = w.kv_first;
     t.s_end = w.kv_first + w.kv_count;
-    if (t.s < t.s_end) t.nx = p.plan.kvsegs[t.s];
+    t.nx = w.kv0;
     return seg_setup(p, w, t);
   }
   if (p.mode == MODE_OWN) {
@@ -318,6 +319,9 @@ __device__ __forceinline__ bool take_unit(const Params& p, uint32_t& k, int& u, 
                                           uint64_t* bars, volatile int* abort, bool single) {
   if (MODE == MODE_FWD) {
     u = blockIdx.x + static_cast<int>(k++) * gridDim.x;
+    // the record of the unit after this one, into L1 while this one runs
+    const int un = u + gridDim.x;
+    if (un < p.n_units) asm volatile("prefetch.global.L1 [%0];" ::"l"(&p.plan.items[un % p.plan.n_items]));
     return true;
   }
   const int slot = k % kURing;

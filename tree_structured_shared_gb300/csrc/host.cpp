@@ -349,7 +349,16 @@ static std::vector<FwdItem> build_items(const padoc_tree_desc* desc, int tile_to
         if (kv.causal) len = std::min<int64_t>(kv.len, t1 - kv.start);
         c += (len + kTileKeys - 1) / kTileKeys;
       }
-      v.push_back({c, {static_cast<int32_t>(s), t0, static_cast<int32_t>(c), 0}});
+      FwdItem it{};
+      it.qseg = static_cast<int32_t>(s);
+      it.tile_start = t0;
+      it.n_tiles = static_cast<int32_t>(c);
+      it.q_end = q.q_start + q.q_len;
+      it.kv_first = q.kv_first;
+      it.kv_count = q.kv_count;
+      it.tile_last = t1 - 1;
+      if (q.kv_count > 0) it.kv0 = desc->kvsegs[q.kv_first];
+      v.push_back({c, it});
     }
   }
   std::stable_sort(v.begin(), v.end(), [](const Cost& a, const Cost& b) { return a.cost > b.cost; });

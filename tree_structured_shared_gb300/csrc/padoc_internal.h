@@ -22,7 +22,10 @@ struct KVSeg {
 struct FwdItem {
   int32_t qseg, tile_start;
   int32_t n_tiles;  // key tiles the tile's walk visits (every kernel role counts on it)
-  int32_t pad;
+  // the query segment's fields and its first key segment, copied so a
+  // kernel reads one record per unit
+  int32_t q_end, kv_first, kv_count, tile_last, pad;
+  KVSeg kv0;
 };
 
 constexpr int kTileKeys = 128;  // keys per K/V tile
