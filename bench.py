@@ -259,10 +259,14 @@ def decode_report(dec, dw, t_pre: float, t_own: float, hbm: float, tf_sus: float
                 "frac_hbm": gbs / hbm, "achieved_tflops": tfs, "frac_tensor": tfs / tf_sus,
                 "bound_time_ms": bound, "frac_of_bound": bound / ms}
 
+    step = dict(part(t_dec, all_b, dec_fl), tokens_per_s=dec.nq / (t_dec * 1e-3),
+                frac_spec_8tbs=all_b / (t_dec * 1e-3) / 1e9 / 8000.0)
+    if dec._plan.fused():
+        # one kernel: the prefix pass call launches nothing
+        return {"fused_pass": dict(part(t_dec, all_b, dec_fl), kernel="attn_tc_kernel<MODE_VERIFY>"),
+                "step": step, "pages": len(dw.pages), "branches": dw.n_branches, "query_tokens": dec.nq}
     return {"prefix_pass": part(t_pre, pre_b, pre_fl), "own_pass": part(t_own, own_b, own_fl),
-            "step": dict(part(t_dec, all_b, dec_fl), tokens_per_s=dec.nq / (t_dec * 1e-3),
-                         frac_spec_8tbs=all_b / (t_dec * 1e-3) / 1e9 / 8000.0),
-            "pages": len(dw.pages), "branches": dw.n_branches, "query_tokens": dec.nq}
+            "step": step, "pages": len(dw.pages), "branches": dw.n_branches, "query_tokens": dec.nq}
 
 
 def main() -> int:
@@ -542,7 +546,7 @@ def main() -> int:
                      "frac": bwd.flops / (t_bwd * 1e-3) / 1e12 / tf_sus, "algorithmic_flops": bwd.flops,
                      "what": "dQ, dK, dV of the same forward (launches: row sums, dQ pass, dK/dV pass)",
                      "traffic": bwd_traffic(fw.n_tokens)},
-        "gpu_launches": ((5 if acc is not None else 3) + 3) * K,
+        "gpu_launches": ((1 if dec._plan.fused() else 2) + (2 if acc is not None else 0) + 1 + 3) * K,
         "clocks": clk,
     }
     if acc is not None:
@@ -561,7 +565,9 @@ def main() -> int:
         sw = sd["w"]
         own_units = sum(sum(pg.own_len) for pg in sw.pages)
         pre_units = sum(max(pg.branch_prefix_len or [0]) for pg in sw.pages)
-        if name == "verify":
+        if "fused_pass" in rep:
+            rep["fused_pass"]["traffic"] = traffic_for("verify_fused", own_units + pre_units)
+        elif name == "verify":
             rep["own_pass"]["kernel"] = "own_kmajor_kernel"
             rep["own_pass"]["traffic"] = traffic_for("own_kmajor_verify", own_units)
             rep["prefix_pass"]["traffic"] = traffic_for("prefix_pass_verify", pre_units)
@@ -577,11 +583,15 @@ def main() -> int:
                              "traffic": traffic_for("accept", a.nq * args.vocab)}
             t_v = rep["step"]["ms"] + t_a
             rep["verify_step"] = {"ms": t_v, "tokens_per_s": sd["dec"].nq * world / (t_v * 1e-3),
-                                  "what": "prefix pass + own pass + accept (row argmax, tree walk at tau 0.75)"}
+                                  "what": ("fused verify pass" if "fused_pass" in rep else "prefix pass + own pass") +
+                                          " + accept (row argmax, tree walk at tau 0.75)"}
         line["kernels"][name] = rep
     if side:
-        # branch decode: prefix + own pass; verify: prefix + own pass + row argmax + tree walk
-        line["gpu_launches"] += (2 * ("branch_decode" in side) + 4 * ("verify" in side)) * K
+        # branch decode: prefix + own pass; verify: the fused pass (or prefix + own pass) + row argmax + tree walk
+        n_side = 2 * ("branch_decode" in side)
+        if "verify" in side:
+            n_side += (1 if side["verify"]["dec"]._plan.fused() else 2) + 2
+        line["gpu_launches"] += n_side * K
     if e2e:
         line["e2e"] = e2e
     if cpu:

@@ -288,6 +288,16 @@ PADOC_API int padoc_branch_decode(padoc_kv_pool* pool, const padoc_decode_batch*
  *                             suffix and the query block under the tree mask,
  *                             then the log-sum-exp merge with kernel 1's
  *                             partials into o and lse
+ *   padoc_decode_plan_fused   *fused = 1 when the plan runs as one kernel: a
+ *                             verify step (Hq / Hkv >= 2, several query rows
+ *                             per branch) whose every page prefix fits one
+ *                             40-tile chunk.  Its prefix pass then launches
+ *                             nothing and its own pass walks, per page, row
+ *                             tile and kv head, the prefix, the own suffixes
+ *                             of the tile's branches and their query block,
+ *                             and writes o and lse directly.  The
+ *                             environment variable PADOC_VERIFY_FUSED=0
+ *                             (read once per process) keeps two kernels.
  * Arguments mean what they mean for padoc_branch_decode; ws must hold the
  * uploaded plan.  The own pass reads what the prefix pass wrote to ws, so
  * run them in this order on one stream. */
@@ -295,6 +305,7 @@ typedef struct padoc_decode_plan padoc_decode_plan;
 PADOC_API int padoc_decode_plan_create(padoc_kv_pool* pool, const padoc_decode_batch* batch, int32_t Hq,
                                        padoc_decode_plan** out);
 PADOC_API int padoc_decode_plan_ws_size(const padoc_decode_plan* plan, size_t* bytes);
+PADOC_API int padoc_decode_plan_fused(const padoc_decode_plan* plan, int32_t* fused);
 PADOC_API int padoc_decode_plan_upload(padoc_decode_plan* plan, void* ws, size_t ws_bytes, padoc_stream_t stream);
 PADOC_API int padoc_decode_prefix_pass(const padoc_decode_plan* plan, const void* q, float scale, void* ws,
                                        padoc_stream_t stream);

@@ -256,3 +256,35 @@ def test_backward_plan_covers_every_pair_once(padoc_lib, seed, order):
                 if hi > k_lo:
                     got[t, k_lo:hi] += 1
     assert np.array_equal(got, want)
+
+
+def _verify_plan(Hq, prefix, q_len, n_branches=3, own=40):
+    """A host-only plan of one page: `prefix` tokens shared by n_branches
+    forks with `own` tokens each and `q_len` query rows per branch."""
+    pool = padoc.KVPool(None, None, 2048, Hkv=2, d=128, max_seqs=16, max_blocks_per_seq=512)
+    page = pool.alloc(prefix)
+    pool.advance(page, prefix)
+    branches = []
+    for _ in range(n_branches):
+        c = pool.fork(page, prefix)
+        pool.reserve(c, own)
+        pool.advance(c, own)
+        branches.append(c)
+    batch = padoc.Batch([page], [0, n_branches], branches, [q_len * i for i in range(n_branches + 1)])
+    return padoc.DecodePlan(pool, batch, Hq), (pool, batch)
+
+
+def test_decode_plan_fusion_decision(padoc_lib):
+    """A verify step runs as one kernel when Hq / Hkv >= 2, each branch
+    stacks enough query rows for the tensor cores, and every page prefix
+    fits one 40-tile chunk (5120 tokens); otherwise as the two passes."""
+    plan, keep = _verify_plan(Hq=4, prefix=700, q_len=8)
+    assert plan.fused()
+    plan, keep = _verify_plan(Hq=4, prefix=5120, q_len=8)
+    assert plan.fused()
+    plan, keep = _verify_plan(Hq=4, prefix=5121, q_len=8)  # 41 key tiles: several chunks
+    assert not plan.fused()
+    plan, keep = _verify_plan(Hq=2, prefix=700, q_len=8)  # one head per kv head
+    assert not plan.fused()
+    plan, keep = _verify_plan(Hq=4, prefix=700, q_len=1)  # decode: one row per branch and head pair
+    assert not plan.fused()

@@ -1234,6 +1234,12 @@ extern "C" int padoc_decode_plan_ws_size(const padoc_decode_plan* plan, size_t* 
   return PADOC_OK;
 }
 
+extern "C" int padoc_decode_plan_fused(const padoc_decode_plan* plan, int32_t* fused) {
+  if (!plan || !fused) return fail(PADOC_ERR_INVALID, "decode_plan_fused: null argument");
+  *fused = plan->pl.fused ? 1 : 0;
+  return PADOC_OK;
+}
+
 static int check_ws(const padoc_decode_plan* plan, const void* ws, size_t ws_bytes) {
   if (!ws) return fail(PADOC_ERR_INVALID, "decode: null workspace");
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(PADOC_ERR_INVALID, "decode: ws must be 256-byte aligned");

@@ -27,7 +27,7 @@ EXPORTED = [
     "padoc_kv_append", "padoc_kv_fork", "padoc_kv_release", "padoc_kv_seq_info", "padoc_kv_seq_blocks",
     "padoc_kv_block_refcount", "padoc_kv_pool_stats", "padoc_kv_pool_sync", "padoc_kv_pool_device",
     "padoc_debug_kv_pool_rehome", "padoc_debug_set_wait_limit", "padoc_branch_decode_ws_size", "padoc_branch_decode", "padoc_tree_mask_build", "padoc_depths",
-    "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_upload",
+    "padoc_device_status", "padoc_decode_plan_create", "padoc_decode_plan_ws_size", "padoc_decode_plan_fused", "padoc_decode_plan_upload",
     "padoc_decode_prefix_pass", "padoc_decode_own_pass", "padoc_decode_plan_free", "padoc_branch_decode_noalloc",
     "padoc_verify_accept", "padoc_kv_commit", "padoc_draft_index_create", "padoc_draft_index_free",
     "padoc_draft_trie", "padoc_draft_trie_batch", "padoc_tree_attn_varlen_bwd_ws_size",
@@ -111,6 +111,7 @@ def lib() -> C.CDLL:
             "padoc_device_status": (C.c_int, [vp]),
             "padoc_decode_plan_create": (C.c_int, [vp, C.POINTER(DecodeBatch), i32, C.POINTER(vp)]),
             "padoc_decode_plan_ws_size": (C.c_int, [vp, C.POINTER(C.c_size_t)]),
+            "padoc_decode_plan_fused": (C.c_int, [vp, C.POINTER(C.c_int32)]),
             "padoc_decode_plan_upload": (C.c_int, [vp, vp, C.c_size_t, vp]),
             "padoc_decode_prefix_pass": (C.c_int, [vp, vp, f32, vp, vp]),
             "padoc_decode_own_pass": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp]),
@@ -525,6 +526,12 @@ class DecodePlan:
         n = C.c_size_t()
         _check(lib().padoc_decode_plan_ws_size(self.handle, C.byref(n)))
         return n.value
+
+    def fused(self) -> bool:
+        """True when the step runs as one kernel (the prefix pass launches nothing)."""
+        f = C.c_int32()
+        _check(lib().padoc_decode_plan_fused(self.handle, C.byref(f)))
+        return bool(f.value)
 
     def upload(self, ws, ws_bytes: int, stream=None):
         _check(lib().padoc_decode_plan_upload(self.handle, _ptr(ws), int(ws_bytes), _stream(stream)))
