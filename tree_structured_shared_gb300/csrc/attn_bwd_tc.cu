@@ -114,31 +114,38 @@ enum {
 };
 
 struct DqUnit {
-  int32_t g, tile_start, q_end, kv_first, kv_count, tile_last;
+  int32_t g, tile_start, q_end, kv_first, kv_count, tile_last, n_tiles;
+  KVSeg kv0;
 };
 
+// One record per unit: the plan item carries its query segment's fields,
+// its first key segment and its key-tile count.
 __device__ __forceinline__ DqUnit dq_unit(const DqParams& p, int u) {
   DqUnit w;
   // head-major: the CTAs at work at one time share one kv head's K/V
   w.g = u / p.plan.n_items;
   const FwdItem it = p.plan.items[u % p.plan.n_items];
-  const QSeg qs = p.plan.qsegs[it.qseg];
   w.tile_start = it.tile_start;
-  w.q_end = qs.q_start + qs.q_len;
-  w.kv_first = qs.kv_first;
-  w.kv_count = qs.kv_count;
-  w.tile_last = min(it.tile_start + p.plan.tile_tokens, w.q_end) - 1;
+  w.q_end = it.q_end;
+  w.kv_first = it.kv_first;
+  w.kv_count = it.kv_count;
+  w.tile_last = it.tile_last;
+  w.n_tiles = it.n_tiles;
+  w.kv0 = it.kv0;
   return w;
 }
 
 // Key tiles of a dQ unit: each key segment in 128-key steps, causal
-// segments cut after the unit's last query.
+// segments cut after the unit's last query.  The next segment's descriptor
+// is loaded on entering a segment (t.nx).
 struct KeyIter {
   int32_t s, ks, end, causal;
+  KVSeg nx;
 };
 __device__ __forceinline__ bool key_setup(const DqParams& p, const DqUnit& w, KeyIter& t) {
   while (t.s < w.kv_first + w.kv_count) {
-    const KVSeg kv = p.plan.kvsegs[t.s];
+    const KVSeg kv = t.nx;
+    if (t.s + 1 < w.kv_first + w.kv_count) t.nx = p.plan.kvsegs[t.s + 1];
     int32_t end = kv.start + kv.len;
     if (kv.causal) end = min(end, w.tile_last + 1);
     if (end > kv.start) {
@@ -153,6 +160,7 @@ __device__ __forceinline__ bool key_setup(const DqParams& p, const DqUnit& w, Ke
 }
 __device__ __forceinline__ bool key_begin(const DqParams& p, const DqUnit& w, KeyIter& t) {
   t.s = w.kv_first;
+  t.nx = w.kv0;
   return key_setup(p, w, t);
 }
 __device__ __forceinline__ bool key_next(const DqParams& p, const DqUnit& w, KeyIter& t) {
@@ -161,12 +169,7 @@ __device__ __forceinline__ bool key_next(const DqParams& p, const DqUnit& w, Key
   ++t.s;
   return key_setup(p, w, t);
 }
-__device__ __forceinline__ int key_count(const DqParams& p, const DqUnit& w) {
-  int n = 0;
-  KeyIter t;
-  for (bool ok = key_begin(p, w, t); ok; ok = key_next(p, w, t)) ++n;
-  return n;
-}
+__device__ __forceinline__ int key_count(const DqParams&, const DqUnit& w) { return w.n_tiles; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -427,6 +430,8 @@ enum {
 };
 
 // Query tiles of a key tile: each entry's queries in steps of tile_tokens.
+// The next entry is prefetched into L1 on entering an entry, so a switch
+// does not wait on L2 or DRAM.
 struct QIter {
   int32_t e, e_end, t0;
   BwdEntry be;
@@ -436,6 +441,7 @@ __device__ __forceinline__ bool q_begin(const DkvParams& p, const BwdItem& it, Q
   q.e_end = it.e_first + it.e_count;
   if (q.e >= q.e_end) return false;
   q.be = p.plan.entries[q.e];
+  if (q.e + 1 < q.e_end) asm volatile("prefetch.global.L1 [%0];" ::"l"(&p.plan.entries[q.e + 1]));
   q.t0 = q.be.q_lo;
   return true;
 }
@@ -444,6 +450,7 @@ __device__ __forceinline__ bool q_next(const DkvParams& p, QIter& q) {
   if (q.t0 < q.be.q_hi) return true;
   if (++q.e >= q.e_end) return false;
   q.be = p.plan.entries[q.e];
+  if (q.e + 1 < q.e_end) asm volatile("prefetch.global.L1 [%0];" ::"l"(&p.plan.entries[q.e + 1]));
   q.t0 = q.be.q_lo;
   return true;
 }
