@@ -214,7 +214,8 @@ PADOC_API int padoc_debug_kv_pool_rehome(padoc_kv_pool* pool, int32_t device);
  *   ws               device workspace of padoc_tree_attn_varlen_bwd_ws_size
  *                    bytes, 256-byte aligned, not in use by a running call
  * dtype PADOC_BF16 or PADOC_F32; d 64 or 128; Hq / Hkv in {1, 2, 4, 8, 16};
- * scale as in the forward.  Results are deterministic (no atomics). */
+ * scale as in the forward.  Results are deterministic: every output row
+ * belongs to one work unit (an atomic counter in ws only hands units out). */
 PADOC_API int padoc_tree_attn_varlen_bwd_ws_size(const padoc_tree_desc* desc, int32_t Hq, size_t* bytes);
 PADOC_API int padoc_tree_attn_varlen_bwd(padoc_tree_desc* desc, const void* q, const void* k, const void* v,
                                          const void* o, const float* lse, const void* d_o, void* dq, void* dk,

@@ -86,6 +86,7 @@ struct DkvParams {
   const float* delta;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  int32_t* work;  // unit counter, zero at launch
 };
 
 // ============================================================ dQ pass
@@ -425,9 +426,33 @@ enum {
   // per query-row half h (columns 64h .. 64h + 63 of S^T and dP^T, warpgroup h):
   KB_PDS_FULL = 7,  // +h, count 4: P^T and dS^T of the half are in TMEM
   KB_ACC_DONE = 9,
-  KB_ACC_FREE = 10,  // count 8
-  KB_N = 11
+  KB_ACC_FREE = 10,   // count 8
+  KB_UNIT_FULL = 11,  // +slot (4): the unit ring's slot holds the next unit
+  KB_UNIT_EMPTY = 15, // +slot (4), count 9: the MMA thread and the element-wise warps read it
+  KB_N = 19
 };
+// Units (key tile, kv head) are drawn in order from a counter in the
+// workspace as CTAs free up (their lengths vary with how many query tiles
+// see the key tile): the producer draws the next unit once the current
+// one's Q / dO copies are issued and publishes it in a ring of kURing slots
+// after the barriers; the MMA thread and the element-wise warps read it there.
+constexpr int kURing = 4;
+constexpr int K_SM_URING = K_SM_BAR + 192;
+static_assert(KB_N * 8 + 8 <= 192, "dK/dV barrier area");
+
+// The next unit of a role that reads the ring (`single`: one thread runs
+// the role); false when a wait gave up.
+__device__ __forceinline__ bool take_unit(uint32_t& k, int& u, volatile int32_t* uring, uint64_t* bars,
+                                          volatile int* abort, bool single) {
+  const int slot = k % kURing;
+  const bool ok = mbar_wait(smem_u32(&bars[KB_UNIT_FULL + slot]), (k / kURing) & 1, abort);
+  if (single ? !ok : !__all_sync(0xffffffffu, ok)) return false;
+  u = uring[slot];
+  if (!single) __syncwarp();
+  if (single || (threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars[KB_UNIT_EMPTY + slot]));
+  ++k;
+  return true;
+}
 
 // Query tiles of a key tile: each entry's queries in steps of tile_tokens.
 // The next entry is prefetched into L1 on entering an entry, so a switch
@@ -468,11 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K_SM_BAR + KB_N * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + K_SM_BAR + KB_N * 8 + 4);
   float* rowdata = reinterpret_cast<float*>(smem + K_SM_ROW);
+  volatile int32_t* uring = reinterpret_cast<volatile int32_t*>(smem + K_SM_URING);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   if (threadIdx.x == 0) {
     for (int i = 0; i < KB_N; ++i)
-      mbar_init(bar(i), (i == KB_PDS_FULL || i == KB_PDS_FULL + 1) ? 4u : (i == KB_ACC_FREE ? 8u : 1u));
+      mbar_init(bar(i), (i == KB_PDS_FULL || i == KB_PDS_FULL + 1)
+                            ? 4u
+                            : (i == KB_ACC_FREE ? 8u : ((i >= KB_UNIT_EMPTY && i < KB_UNIT_EMPTY + kURing) ? 9u : 1u)));
     *abort = 0;
     fence_mbar_init();
   }
@@ -496,12 +524,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint32_t qd_it = 0, unit_it = 0;
     bool failed = false;
-    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+    // draw a unit and publish it in the ring (-1 when a wait gave up)
+    uint32_t n_pub = 0;
+    auto publish = [&]() -> int {
+      const int slot = n_pub % kURing;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_UNIT_EMPTY + slot), ((n_pub / kURing) & 1) ^ 1, abort)))
+        return -1;
+      int v = 0;
+      if (lane == 0) {
+        v = atomicAdd(p.work, 1);
+        uring[slot] = v;
+        mbar_arrive(bar(KB_UNIT_FULL + slot));
+      }
+      ++n_pub;
+      return __shfl_sync(0xffffffffu, v, 0);
+    };
+    int u_next = publish();
+    if (u_next < 0) failed = true;
+    while (!failed) {
+      const int u = u_next;
+      if (u >= p.n_units) break;
       // head-major: the CTAs at work at one time share one kv head's Q / dO
       const BwdItem it = p.plan.items[u % p.plan.n_items];
       const int g = u / p.plan.n_items;
       QIter q;
-      if (!q_begin(p, it, q)) continue;
+      if (!q_begin(p, it, q)) {
+        u_next = publish();
+        if (u_next < 0) failed = true;
+        continue;
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_KV_EMPTY), (unit_it & 1) ^ 1, abort))) { failed = true; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(KB_KV_FULL), 2 * kTile);
@@ -538,6 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
       }
+      if (failed) break;
+      u_next = publish();
+      if (u_next < 0) {
+        failed = true;
+        break;
+      }
       ++unit_it;
     }
     if (failed && lane == 0) raise_abort(abort, 0x100);
@@ -570,7 +627,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + K_T_DP, kmajor_step(d_v, kk), kmajor_step(ddo, kk), id_kk, kk > 0);
         mma_commit(bar(KB_SP_FULL));
       };
-      for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+      uint32_t n_taken = 0;
+      while (!failed) {
+        int u;
+        if (!take_unit(n_taken, u, uring, bars, abort, true)) {
+          failed = true;
+          break;
+        }
+        if (u >= p.n_units) break;
         const BwdItem it = p.plan.items[u % p.plan.n_items];
         QIter q;
         if (!q_begin(p, it, q)) continue;
@@ -631,7 +695,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t qd_it = 0, g_it = 0, unit_it = 0;
     bool failed = false;
-    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+    uint32_t n_taken = 0;
+    while (!failed) {
+      int u;
+      if (!take_unit(n_taken, u, uring, bars, abort, false)) {
+        failed = true;
+        break;
+      }
+      if (u >= p.n_units) break;
       // head-major: the CTAs at work at one time share one kv head's Q / dO
       const BwdItem it = p.plan.items[u % p.plan.n_items];
       const int g = u / p.plan.n_items;
@@ -810,6 +881,15 @@ int launch_bwd_tc(const BwdArgs& a, cudaStream_t s, std::string* err) {
   }
   if (a.bwd.n_items > 0) {
     DkvParams p{};
+    p.work = a.work;
+    {
+      // units are drawn from this counter in order
+      const cudaError_t e = cudaMemsetAsync(a.work, 0, sizeof(int32_t), s);
+      if (e != cudaSuccess) {
+        *err = std::string("cudaMemsetAsync of the unit counter: ") + cudaGetErrorString(e);
+        return PADOC_ERR_CUDA;
+      }
+    }
     p.plan = a.bwd;
     p.n_units = a.bwd.n_items * a.Hkv;
     p.Hq = a.Hq;

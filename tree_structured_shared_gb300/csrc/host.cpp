@@ -465,9 +465,11 @@ extern "C" int padoc_tree_attn_varlen(padoc_tree_desc* desc, const void* q, cons
   return PADOC_OK;
 }
 
-static size_t bwd_ws_bytes(const padoc_tree_desc* desc, int32_t Hq) {
+// rowsum(dO * O) [Hq, T] f32, then the dK/dV pass's unit counter
+static size_t bwd_delta_bytes(const padoc_tree_desc* desc, int32_t Hq) {
   return (static_cast<size_t>(Hq) * desc->T * sizeof(float) + 255) / 256 * 256;
 }
+static size_t bwd_ws_bytes(const padoc_tree_desc* desc, int32_t Hq) { return bwd_delta_bytes(desc, Hq) + 256; }
 
 extern "C" int padoc_tree_attn_varlen_bwd_ws_size(const padoc_tree_desc* desc, int32_t Hq, size_t* bytes) {
   if (!desc || !bytes) return fail(PADOC_ERR_INVALID, "tree_attn_varlen_bwd_ws_size: null argument");
@@ -513,6 +515,7 @@ extern "C" int padoc_tree_attn_varlen_bwd(padoc_tree_desc* desc, const void* q, 
   a.dk = dk;
   a.dv = dv;
   a.delta = static_cast<float*>(ws);
+  a.work = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + bwd_delta_bytes(desc, Hq));
   a.T = desc->T;
   a.Hq = Hq;
   a.Hkv = Hkv;

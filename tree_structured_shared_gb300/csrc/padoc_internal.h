@@ -85,6 +85,7 @@ struct BwdArgs {
   void* dk;
   void* dv;
   float* delta;       // workspace [Hq, T]: rowsum(dO * O)
+  int32_t* work;      // workspace: unit counter of the dK/dV pass (zeroed by its launcher)
   int64_t T;
   int32_t Hq, Hkv, d;
   float scale;
