@@ -74,6 +74,7 @@ struct DqParams {
   const float* lse;
   const float* delta;
   __nv_bfloat16* dq;
+  int32_t* work;  // unit counter, zero at launch
 };
 
 struct DkvParams {
@@ -88,6 +89,27 @@ struct DkvParams {
   __nv_bfloat16* dv;
   int32_t* work;  // unit counter, zero at launch
 };
+
+// Both passes draw their units in order from a counter in the workspace as
+// CTAs free up: the producer draws the next unit once the current one's
+// copies are issued and publishes it in a ring of kURing slots after the
+// barriers; the MMA thread and the element-wise warps read it there.
+constexpr int kURing = 4;
+
+// The next unit of a role that reads the ring (`single`: one thread runs
+// the role; full / empty: the slots' barrier indices); false when a wait
+// gave up.
+__device__ __forceinline__ bool take_unit(uint32_t& k, int& u, volatile int32_t* uring, uint64_t* bars, int full,
+                                          int empty, volatile int* abort, bool single) {
+  const int slot = k % kURing;
+  const bool ok = mbar_wait(smem_u32(&bars[full + slot]), (k / kURing) & 1, abort);
+  if (single ? !ok : !__all_sync(0xffffffffu, ok)) return false;
+  u = uring[slot];
+  if (!single) __syncwarp();
+  if (single || (threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars[empty + slot]));
+  ++k;
+  return true;
+}
 
 // ============================================================ dQ pass
 // smem: Q | dO | K ring (2) | V ring (2) | barriers
@@ -111,8 +133,12 @@ enum {
   QB_DQ_DONE = 10,  // +h: dQ += dS K over the half has run (the dS columns are free)
   QB_DQ_ALL = 12,   // the unit's dQ is complete
   QB_ACC_FREE = 13,  // count 8: the epilogue has read dQ
-  QB_N = 14
+  QB_UNIT_FULL = 14,   // +slot (4): the unit ring's slot holds the next unit
+  QB_UNIT_EMPTY = 18,  // +slot (4), count 9: the MMA thread and the element-wise warps read it
+  QB_N = 22
 };
+constexpr int Q_SM_URING = Q_SM_BAR + 192;
+static_assert(QB_N * 8 + 8 <= 192, "dQ barrier area");
 
 struct DqUnit {
   int32_t g, tile_start, q_end, kv_first, kv_count, tile_last, n_tiles;
@@ -184,11 +210,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Q_SM_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Q_SM_BAR + QB_N * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + Q_SM_BAR + QB_N * 8 + 4);
+  volatile int32_t* uring = reinterpret_cast<volatile int32_t*>(smem + Q_SM_URING);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_N; ++i)
-      mbar_init(bar(i), (i == QB_DS_FULL || i == QB_DS_FULL + 1) ? 4u : ((i == QB_ACC_FREE || i == QB_RD) ? 8u : 1u));
+      mbar_init(bar(i), (i == QB_DS_FULL || i == QB_DS_FULL + 1)
+                            ? 4u
+                            : ((i == QB_ACC_FREE || i == QB_RD) ? 8u
+                                                                : ((i >= QB_UNIT_EMPTY && i < QB_UNIT_EMPTY + kURing) ? 9u : 1u)));
     *abort = 0;
     fence_mbar_init();
   }
@@ -211,9 +241,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
       uint32_t kv_it = 0, unit_it = 0;
       bool failed = false;
-      for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+      // draw a unit and publish it in the ring (-1 when a wait gave up)
+      uint32_t n_pub = 0;
+      auto publish = [&]() -> int {
+        const int slot = n_pub % kURing;
+        if (!mbar_wait(bar(QB_UNIT_EMPTY + slot), ((n_pub / kURing) & 1) ^ 1, abort)) return -1;
+        const int v = atomicAdd(p.work, 1);
+        uring[slot] = v;
+        mbar_arrive(bar(QB_UNIT_FULL + slot));
+        ++n_pub;
+        return v;
+      };
+      int u_next = publish();
+      if (u_next < 0) failed = true;
+      while (!failed) {
+        const int u = u_next;
+        if (u >= p.n_units) break;
         const DqUnit w = dq_unit(p, u);
-        if (key_count(p, w) == 0) continue;
+        if (key_count(p, w) == 0) {
+          u_next = publish();
+          if (u_next < 0) failed = true;
+          continue;
+        }
         if (!mbar_wait(bar(QB_QD_EMPTY), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
         mbar_arrive_expect_tx(bar(QB_QD_FULL), 2 * kTile);
         for (int hh = 0; hh < G; ++hh)
@@ -232,6 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sbase + Q_SM_K + st * kTile + h * kHalf, &tm_k, bar(QB_KV_FULL + st), h * 64, w.g, t.ks);
             tma_load_3d(sbase + Q_SM_V + st * kTile + h * kHalf, &tm_v, bar(QB_KV_FULL + st), h * 64, w.g, t.ks);
           }
+        }
+        if (failed) break;
+        u_next = publish();
+        if (u_next < 0) {
+          failed = true;
+          break;
         }
         ++unit_it;
       }
@@ -271,7 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last) mma_commit(bar(QB_DQ_ALL));
         return true;
       };
-      for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+      uint32_t n_taken = 0;
+      while (!failed) {
+        int u;
+        if (!take_unit(n_taken, u, uring, bars, QB_UNIT_FULL, QB_UNIT_EMPTY, abort, true)) {
+          failed = true;
+          break;
+        }
+        if (u >= p.n_units) break;
         const DqUnit w = dq_unit(p, u);
         const int n = key_count(p, w);
         if (n == 0) continue;
@@ -307,7 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t g_it = 0, unit_it = 0;
     bool failed = false;
-    for (int u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+    uint32_t n_taken = 0;
+    while (!failed) {
+      int u;
+      if (!take_unit(n_taken, u, uring, bars, QB_UNIT_FULL, QB_UNIT_EMPTY, abort, false)) {
+        failed = true;
+        break;
+      }
+      if (u >= p.n_units) break;
       const DqUnit w = dq_unit(p, u);
       const int n = key_count(p, w);
       if (n == 0) continue;
@@ -431,28 +500,11 @@ enum {
   KB_UNIT_EMPTY = 15, // +slot (4), count 9: the MMA thread and the element-wise warps read it
   KB_N = 19
 };
-// Units (key tile, kv head) are drawn in order from a counter in the
-// workspace as CTAs free up (their lengths vary with how many query tiles
-// see the key tile): the producer draws the next unit once the current
-// one's Q / dO copies are issued and publishes it in a ring of kURing slots
-// after the barriers; the MMA thread and the element-wise warps read it there.
-constexpr int kURing = 4;
+// The units (key tile, kv head) vary with how many query tiles see the key
+// tile; the ring sits after the barriers.
 constexpr int K_SM_URING = K_SM_BAR + 192;
 static_assert(KB_N * 8 + 8 <= 192, "dK/dV barrier area");
 
-// The next unit of a role that reads the ring (`single`: one thread runs
-// the role); false when a wait gave up.
-__device__ __forceinline__ bool take_unit(uint32_t& k, int& u, volatile int32_t* uring, uint64_t* bars,
-                                          volatile int* abort, bool single) {
-  const int slot = k % kURing;
-  const bool ok = mbar_wait(smem_u32(&bars[KB_UNIT_FULL + slot]), (k / kURing) & 1, abort);
-  if (single ? !ok : !__all_sync(0xffffffffu, ok)) return false;
-  u = uring[slot];
-  if (!single) __syncwarp();
-  if (single || (threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars[KB_UNIT_EMPTY + slot]));
-  ++k;
-  return true;
-}
 
 // Query tiles of a key tile: each entry's queries in steps of tile_tokens.
 // The next entry is prefetched into L1 on entering an entry, so a switch
@@ -630,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n_taken = 0;
       while (!failed) {
         int u;
-        if (!take_unit(n_taken, u, uring, bars, abort, true)) {
+        if (!take_unit(n_taken, u, uring, bars, KB_UNIT_FULL, KB_UNIT_EMPTY, abort, true)) {
           failed = true;
           break;
         }
@@ -698,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n_taken = 0;
     while (!failed) {
       int u;
-      if (!take_unit(n_taken, u, uring, bars, abort, false)) {
+      if (!take_unit(n_taken, u, uring, bars, KB_UNIT_FULL, KB_UNIT_EMPTY, abort, false)) {
         failed = true;
         break;
       }
@@ -866,6 +918,14 @@ int launch_bwd_tc(const BwdArgs& a, cudaStream_t s, std::string* err) {
   const float sl2 = a.scale * kLog2e;
   if (a.fwd.n_items > 0) {
     DqParams p{};
+    p.work = a.work + 1;  // the dK/dV pass counts in a.work[0]
+    {
+      const cudaError_t e = cudaMemsetAsync(p.work, 0, sizeof(int32_t), s);
+      if (e != cudaSuccess) {
+        *err = std::string("cudaMemsetAsync of the unit counter: ") + cudaGetErrorString(e);
+        return PADOC_ERR_CUDA;
+      }
+    }
     p.plan = a.fwd;
     p.n_units = a.fwd.n_items * a.Hkv;
     p.Hq = a.Hq;
