@@ -115,30 +115,37 @@ __device__ __forceinline__ bool take_unit(uint32_t& k, int& u, volatile int32_t*
 // smem: Q | dO | K ring (2) | V ring (2) | barriers
 constexpr int Q_SM_Q = 0;
 constexpr int Q_SM_DO = kTile;
+// K is read by S (early in a tile's period) and by dQ (late), V only by dP:
+// a three-stage K ring and a two-stage V ring whose stage frees after dP
+// give both a tile's lead over their L2 fetch.
+constexpr int kDqKStages = 3, kDqVStages = 2;
 constexpr int Q_SM_K = 2 * kTile;
-constexpr int Q_SM_V = Q_SM_K + 2 * kTile;
-constexpr int Q_SM_BAR = Q_SM_V + 2 * kTile;
+constexpr int Q_SM_V = Q_SM_K + kDqKStages * kTile;
+constexpr int Q_SM_BAR = Q_SM_V + kDqVStages * kTile;
 constexpr int kDqSmem = Q_SM_BAR + 256 + 1024;
 // TMEM columns
 constexpr uint32_t Q_T_S = 0, Q_T_DP = 128, Q_T_DS = 256, Q_T_DQ = 384;
 enum {
   QB_QD_FULL = 0,
   QB_QD_EMPTY = 1,
-  QB_KV_FULL = 2,   // +stage (2)
-  QB_KV_EMPTY = 4,  // +stage (2)
-  QB_SP_FULL = 6,   // S and dP of the tile are in TMEM
-  QB_RD = 7,        // count 8: both warpgroups have read them (the columns are free)
+  QB_K_FULL = 2,    // +stage (3)
+  QB_K_EMPTY = 5,   // +stage (3): the tile's dQ has run
+  QB_V_FULL = 8,    // +stage (2)
+  QB_V_EMPTY = 10,  // +stage (2): the tile's dP has run
+  QB_SP_FULL = 12,  // S and dP of the tile are in TMEM
+  QB_RD = 13,       // count 8: both warpgroups have read them (the columns are free)
   // per key half h (columns 64h .. 64h + 63 of S and dP, warpgroup h):
-  QB_DS_FULL = 8,   // +h, count 4: dS of the half is in TMEM
-  QB_DQ_DONE = 10,  // +h: dQ += dS K over the half has run (the dS columns are free)
-  QB_DQ_ALL = 12,   // the unit's dQ is complete
-  QB_ACC_FREE = 13,  // count 8: the epilogue has read dQ
-  QB_UNIT_FULL = 14,   // +slot (4): the unit ring's slot holds the next unit
-  QB_UNIT_EMPTY = 18,  // +slot (4), count 9: the MMA thread and the element-wise warps read it
-  QB_N = 22
+  QB_DS_FULL = 14,  // +h, count 4: dS of the half is in TMEM
+  QB_DQ_DONE = 16,  // +h: dQ += dS K over the half has run (the dS columns are free)
+  QB_DQ_ALL = 18,   // the unit's dQ is complete
+  QB_ACC_FREE = 19,  // count 8: the epilogue has read dQ
+  QB_UNIT_FULL = 20,   // +slot (4): the unit ring's slot holds the next unit
+  QB_UNIT_EMPTY = 24,  // +slot (4), count 9: the MMA thread and the element-wise warps read it
+  QB_N = 28
 };
-constexpr int Q_SM_URING = Q_SM_BAR + 192;
-static_assert(QB_N * 8 + 8 <= 192, "dQ barrier area");
+constexpr int Q_SM_URING = Q_SM_BAR + 240;
+static_assert(QB_N * 8 + 8 <= 240, "dQ barrier area");
+static_assert(kDqSmem <= 232448, "dQ pass shared memory");
 
 struct DqUnit {
   int32_t g, tile_start, q_end, kv_first, kv_count, tile_last, n_tiles;
@@ -274,13 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         KeyIter t;
         for (bool ok = key_begin(p, w, t); ok; ok = key_next(p, w, t), ++kv_it) {
-          const int st = kv_it & 1;
-          if (!mbar_wait(bar(QB_KV_EMPTY + st), ((kv_it >> 1) & 1) ^ 1, abort)) { failed = true; break; }
-          mbar_arrive_expect_tx(bar(QB_KV_FULL + st), 2 * kTile);
-          for (int h = 0; h < 2; ++h) {
-            tma_load_3d(sbase + Q_SM_K + st * kTile + h * kHalf, &tm_k, bar(QB_KV_FULL + st), h * 64, w.g, t.ks);
-            tma_load_3d(sbase + Q_SM_V + st * kTile + h * kHalf, &tm_v, bar(QB_KV_FULL + st), h * 64, w.g, t.ks);
-          }
+          const int ks = kv_it % kDqKStages, vs = kv_it % kDqVStages;
+          if (!mbar_wait(bar(QB_K_EMPTY + ks), ((kv_it / kDqKStages) & 1) ^ 1, abort)) { failed = true; break; }
+          mbar_arrive_expect_tx(bar(QB_K_FULL + ks), kTile);
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(sbase + Q_SM_K + ks * kTile + h * kHalf, &tm_k, bar(QB_K_FULL + ks), h * 64, w.g, t.ks);
+          if (!mbar_wait(bar(QB_V_EMPTY + vs), ((kv_it / kDqVStages) & 1) ^ 1, abort)) { failed = true; break; }
+          mbar_arrive_expect_tx(bar(QB_V_FULL + vs), kTile);
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(sbase + Q_SM_V + vs * kTile + h * kHalf, &tm_v, bar(QB_V_FULL + vs), h * 64, w.g, t.ks);
         }
         if (failed) break;
         u_next = publish();
@@ -301,16 +310,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool failed = false;
       // base descriptors: Q and dO (K-major), K and V of each stage (K-major), K as MN-major B
       const uint64_t d_q = sdesc_sw128(sbase + Q_SM_Q, 16, 1024), d_do = sdesc_sw128(sbase + Q_SM_DO, 16, 1024);
-      const uint64_t d_k0 = sdesc_sw128(sbase + Q_SM_K, 16, 1024), d_k1 = sdesc_sw128(sbase + Q_SM_K + kTile, 16, 1024);
+      const uint64_t d_k0 = sdesc_sw128(sbase + Q_SM_K, 16, 1024), d_k1 = sdesc_sw128(sbase + Q_SM_K + kTile, 16, 1024),
+                     d_k2 = sdesc_sw128(sbase + Q_SM_K + 2 * kTile, 16, 1024);
       const uint64_t d_v0 = sdesc_sw128(sbase + Q_SM_V, 16, 1024), d_v1 = sdesc_sw128(sbase + Q_SM_V + kTile, 16, 1024);
       const uint64_t d_kmn0 = sdesc_sw128(sbase + Q_SM_K, kHalf, 1024);
       const uint64_t d_kmn1 = sdesc_sw128(sbase + Q_SM_K + kTile, kHalf, 1024);
+      const uint64_t d_kmn2 = sdesc_sw128(sbase + Q_SM_K + 2 * kTile, kHalf, 1024);
       auto issue_dq = [&](uint32_t tile_it, bool first, bool last) -> bool {
         // dQ += dS K for tile tile_it (dS in TMEM, K of its stage as MN-major
         // B), one key half at a time as each warpgroup finishes its dS
         if (first && !mbar_wait_relaxed(bar(QB_ACC_FREE), (unit_it & 1) ^ 1, abort)) return false;
-        const int st = tile_it & 1;
-        const uint64_t kd = st ? d_kmn1 : d_kmn0;
+        const int st = tile_it % kDqKStages;
+        const uint64_t kd = st == 0 ? d_kmn0 : (st == 1 ? d_kmn1 : d_kmn2);
         for (int half = 0; half < 2; ++half) {
           if (!mbar_wait_relaxed(bar(QB_DS_FULL + half), tile_it & 1, abort)) return false;
           tc_fence_after();
@@ -322,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(bar(QB_DQ_DONE + half));
         }
-        mma_commit(bar(QB_KV_EMPTY + st));
+        mma_commit(bar(QB_K_EMPTY + st));
         if (last) mma_commit(bar(QB_DQ_ALL));
         return true;
       };
@@ -339,9 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n == 0) continue;
         if (!mbar_wait_relaxed(bar(QB_QD_FULL), unit_it & 1, abort)) { failed = true; break; }
         for (int j = 0; j < n; ++j, ++kv_it, ++g_it) {
-          const int st = kv_it & 1;
-          if (!mbar_wait_relaxed(bar(QB_KV_FULL + st), (kv_it >> 1) & 1, abort)) { failed = true; break; }
-          const uint64_t dk = st ? d_k1 : d_k0, dv = st ? d_v1 : d_v0;
+          const int ks = kv_it % kDqKStages, vs = kv_it % kDqVStages;
+          if (!mbar_wait_relaxed(bar(QB_K_FULL + ks), (kv_it / kDqKStages) & 1, abort)) { failed = true; break; }
+          if (!mbar_wait_relaxed(bar(QB_V_FULL + vs), (kv_it / kDqVStages) & 1, abort)) { failed = true; break; }
+          const uint64_t dk = ks == 0 ? d_k0 : (ks == 1 ? d_k1 : d_k2), dv = vs ? d_v1 : d_v0;
           // S and dP go over columns both warpgroups have read (they compute the
           // previous tile's dS from registers meanwhile)
           if (g_it > 0 && !mbar_wait_relaxed(bar(QB_RD), (g_it - 1) & 1, abort)) { failed = true; break; }
@@ -353,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ss(tmem + Q_T_DP, kmajor_step(d_do, kk), kmajor_step(dv, kk), id_kk, kk > 0);
           mma_commit(bar(QB_SP_FULL));
+          mma_commit(bar(QB_V_EMPTY + vs));  // dP has read V
           if (j == n - 1) mma_commit(bar(QB_QD_EMPTY));
           if (j > 0 && !issue_dq(g_it - 1, j == 1, false)) { failed = true; break; }
         }
