@@ -118,12 +118,14 @@ struct padoc_tree_desc {
 };
 
 // Transposes the query segments' key lists onto the global key-tile grid
-// (the key-stationary half of the backward); tiles in LPT order by the
-// (query, key) pairs they hold.
+// (the key-stationary half of the backward).  Tiles stay in position order:
+// the kernel draws them in order as CTAs free up, so the CTAs at work at one
+// time hold key tiles of one page and share its queries' Q and dO in L2
+// (a kv head's Q and dO exceed L2); a page's prefix tiles, seen by the most
+// queries, come before its content tiles.
 static void build_bwd(padoc_tree_desc* desc) {
   const int64_t ntiles = (desc->T + kTileKeys - 1) / kTileKeys;
   std::vector<std::vector<BwdEntry>> per(ntiles);
-  std::vector<int64_t> cost(ntiles, 0);
   for (const QSeg& s : desc->qsegs) {
     for (int32_t j = 0; j < s.kv_count; ++j) {
       const KVSeg& e = desc->kvsegs[s.kv_first + j];
@@ -137,14 +139,12 @@ static void build_bwd(padoc_tree_desc* desc) {
         b.q_hi = s.q_start + s.q_len;
         if (b.q_lo >= b.q_hi) continue;
         per[i].push_back(b);
-        cost[i] += static_cast<int64_t>(b.q_hi - b.q_lo) * (b.k_hi - b.k_lo);
       }
     }
   }
   std::vector<int64_t> order;
   for (int64_t i = 0; i < ntiles; ++i)
     if (!per[i].empty()) order.push_back(i);
-  std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return cost[a] > cost[b]; });
   desc->bitems.clear();
   desc->bentries.clear();
   for (int64_t i : order) {
