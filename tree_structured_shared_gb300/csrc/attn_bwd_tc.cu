@@ -499,19 +499,27 @@ constexpr int K_SM_ROW = K_SM_QD + 4 * kTile;
 constexpr int K_SM_BAR = K_SM_ROW + 2 * 1024;
 constexpr int kDkvSmem = K_SM_BAR + 256 + 1024;
 constexpr uint32_t K_T_S = 0, K_T_DP = 128, K_T_DV = 256, K_T_DK = 384;
+// Per query tile i the MMA thread issues dP^T(i), dV(i) += P^T(i) dO(i),
+// S^T(i+1) and, once dS^T(i) is in, dK(i) += dS^T(i) Q(i).  P^T(i) lives over
+// S^T(i)'s columns and dS^T(i) over dP^T(i)'s; S^T(i+1) is issued after dV(i)
+// and dP^T(i+1) after dK(i), and tensor operations run in issue order, so
+// each overwrites its columns only after they were read.  The element-wise
+// warps compute P^T(i) (phase 1, while dK(i-1) runs) and dS^T(i) (phase 2,
+// while dV(i) and S^T(i+1) run), keeping P in registers between the two.
 enum {
   KB_KV_FULL = 0,
   KB_KV_EMPTY = 1,
   KB_QD_FULL = 2,   // +stage (2)
   KB_QD_EMPTY = 4,  // +stage (2)
-  KB_SP_FULL = 6,   // S^T and dP^T of the tile are in TMEM
-  // per query-row half h (columns 64h .. 64h + 63 of S^T and dP^T, warpgroup h):
-  KB_PDS_FULL = 7,  // +h, count 4: P^T and dS^T of the half are in TMEM
-  KB_ACC_DONE = 9,
-  KB_ACC_FREE = 10,   // count 8
-  KB_UNIT_FULL = 11,  // +slot (4): the unit ring's slot holds the next unit
-  KB_UNIT_EMPTY = 15, // +slot (4), count 9: the MMA thread and the element-wise warps read it
-  KB_N = 19
+  KB_S_FULL = 6,    // S^T of the tile is in TMEM
+  KB_P_FULL = 7,    // count 8: P^T of the tile is in TMEM
+  KB_DP_FULL = 8,   // dP^T of the tile is in TMEM
+  KB_DS_FULL = 9,   // count 8: dS^T of the tile is in TMEM
+  KB_ACC_DONE = 10,
+  KB_ACC_FREE = 11,   // count 8
+  KB_UNIT_FULL = 12,  // +slot (4): the unit ring's slot holds the next unit
+  KB_UNIT_EMPTY = 16, // +slot (4), count 9: the MMA thread and the element-wise warps read it
+  KB_N = 20
 };
 // The units (key tile, kv head) vary with how many query tiles see the key
 // tile; the ring sits after the barriers.
@@ -563,9 +571,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   if (threadIdx.x == 0) {
     for (int i = 0; i < KB_N; ++i)
-      mbar_init(bar(i), (i == KB_PDS_FULL || i == KB_PDS_FULL + 1)
-                            ? 4u
-                            : (i == KB_ACC_FREE ? 8u : ((i >= KB_UNIT_EMPTY && i < KB_UNIT_EMPTY + kURing) ? 9u : 1u)));
+      mbar_init(bar(i), (i == KB_P_FULL || i == KB_DS_FULL || i == KB_ACC_FREE)
+                            ? 8u
+                            : ((i >= KB_UNIT_EMPTY && i < KB_UNIT_EMPTY + kURing) ? 9u : 1u));
     *abort = 0;
     fence_mbar_init();
   }
@@ -682,15 +690,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         d_qmn[st] = sdesc_sw128(qa, kHalf, 1024);
         d_domn[st] = sdesc_sw128(qa + kTile, kHalf, 1024);
       }
-      // S^T = K Q^T and dP^T = V dO^T for the tile in stage st
+      // S^T = K Q^T for the tile in stage st
       auto issue_s = [&](int st) {
-        const uint64_t dq = st ? d_q[1] : d_q[0], ddo = st ? d_do[1] : d_do[0];
+        const uint64_t dq = st ? d_q[1] : d_q[0];
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_bf16_ss(tmem + K_T_S, kmajor_step(d_k, kk), kmajor_step(dq, kk), id_kk, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tmem + K_T_DP, kmajor_step(d_v, kk), kmajor_step(ddo, kk), id_kk, kk > 0);
-        mma_commit(bar(KB_SP_FULL));
+        mma_commit(bar(KB_S_FULL));
       };
       uint32_t n_taken = 0;
       while (!failed) {
@@ -711,32 +716,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (bool ok = true; ok; ++qd_it) {
           const int st = qd_it & 1;
           const uint64_t dqm = st ? d_qmn[1] : d_qmn[0], ddom = st ? d_domn[1] : d_domn[0];
+          const uint64_t ddo = st ? d_do[1] : d_do[0];
           const bool more = q_next(p, q);
           if (first && !mbar_wait_relaxed(bar(KB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
-          for (int half = 0; half < 2; ++half) {
-            // dV += P^T dO and dK += dS^T Q over the half's query rows (warpgroup
-            // h packed rows 64h .. 64h + 63 into columns 64h .. 64h + 31)
-            if (!mbar_wait_relaxed(bar(KB_PDS_FULL + half), qd_it & 1, abort)) { failed = true; break; }
+          if (!mbar_wait_relaxed(bar(KB_P_FULL), qd_it & 1, abort)) { failed = true; break; }
+          tc_fence_after();
+          // dP^T = V dO^T over the columns of dS^T of the tile before (read
+          // by its dK, issued earlier)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + K_T_DP, kmajor_step(d_v, kk), kmajor_step(ddo, kk), id_kk, kk > 0);
+          mma_commit(bar(KB_DP_FULL));
+          // dV += P^T dO (warpgroup h packed query rows 64h .. 64h + 63 into
+          // columns 64h .. 64h + 31)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tmem + K_T_DV, tmem + K_T_S + (kk >> 2) * 64 + (kk & 3) * 8, mnmajor_step(ddom, kk), id_mn,
+                        (!first || kk > 0) ? 1u : 0u);
+          // The next tile's S^T over the columns dV has just read: now, so
+          // that it runs while the element-wise warps compute dS^T, when its
+          // Q has landed; otherwise after dK, so as not to hold dK up.
+          const uint32_t nb = KB_QD_FULL + ((qd_it + 1) & 1), nph = ((qd_it + 1) >> 1) & 1;
+          const bool s_early = more && mbar_test_wait(bar(nb), nph);
+          if (s_early) {
             tc_fence_after();
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-              const int kk = half * 4 + k4;
-              mma_bf16_ts(tmem + K_T_DV, tmem + K_T_S + half * 64 + k4 * 8, mnmajor_step(ddom, kk), id_mn,
-                          (!first || kk > 0) ? 1u : 0u);
-            }
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-              const int kk = half * 4 + k4;
-              mma_bf16_ts(tmem + K_T_DK, tmem + K_T_DP + half * 64 + k4 * 8, mnmajor_step(dqm, kk), id_mn,
-                          (!first || kk > 0) ? 1u : 0u);
-            }
+            issue_s((qd_it + 1) & 1);
           }
-          if (failed) break;
+          if (!mbar_wait_relaxed(bar(KB_DS_FULL), qd_it & 1, abort)) { failed = true; break; }
+          tc_fence_after();
+          // dK += dS^T Q
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tmem + K_T_DK, tmem + K_T_DP + (kk >> 2) * 64 + (kk & 3) * 8, mnmajor_step(dqm, kk), id_mn,
+                        (!first || kk > 0) ? 1u : 0u);
           mma_commit(bar(KB_QD_EMPTY + st));
-          // the next tile's S^T / dP^T over the columns just consumed (the
-          // products above read them first: tensor operations run in order)
-          if (more) {
-            if (!mbar_wait_relaxed(bar(KB_QD_FULL + ((qd_it + 1) & 1)), ((qd_it + 1) >> 1) & 1, abort)) {
+          if (more && !s_early) {
+            if (!mbar_wait_relaxed(bar(nb), nph, abort)) {
               failed = true;
               break;
             }
@@ -780,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           failed = true;
           break;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_SP_FULL), qd_it & 1, abort))) { failed = true; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_S_FULL), qd_it & 1, abort))) { failed = true; break; }
         tc_fence_after();
         const float* rd = rowdata + (qd_it & 1) * 256 + wg * 64;
         // row c (token t0 + c % tt) sees this key iff the token index i = c % tt
@@ -790,63 +805,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i_hi = key_ok ? min(tt, q.be.q_hi - q.t0) : 0;
         // every row of the tile sees every key of the warp: no masks
         const bool all_visible = __all_sync(0xffffffffu, i_lo == 0 && i_hi == tt);
-        const uint64_t sl2x2 = f2pack(p.sl2, p.sl2);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sv[32], dv[32], pp[16], dd[16];
-          tmem_ld32(tmem + lb + K_T_S + wg * 64 + c * 32, sv);
-          tmem_ld32(tmem + lb + K_T_DP + wg * 64 + c * 32, dv);
+        // phase 1: P^T = 2^(S^T sl2 - LSE2) over this warpgroup's 64 query
+        // rows, kept in registers for phase 2 and written as bf16 pairs over
+        // the first 32 of those columns
+        float pf[64];
+        {
+          uint32_t sv[2][32];
+          tmem_ld32(tmem + lb + K_T_S + wg * 64, sv[0]);
+          tmem_ld32(tmem + lb + K_T_S + wg * 64 + 32, sv[1]);
           tmem_wait_ld();
-          const float4* l4 = reinterpret_cast<const float4*>(rd) + c * 8;       // LSE (log2) of the chunk's rows
-          const float4* d4 = reinterpret_cast<const float4*>(rd + 128) + c * 8;  // D of the chunk's rows
+          const float4* l4 = reinterpret_cast<const float4*>(rd);  // LSE (log2) of the rows
           if (all_visible) {
+            const uint64_t sl2x2 = f2pack(p.sl2, p.sl2);
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 l = l4[i >> 2], dl = d4[i >> 2];
-              // two lanes per instruction: x = s * sl2 - LSE2, P = 2^x, dS = P (dP - D)
+            for (int i = 0; i < 64; i += 4) {
+              const float4 l = l4[i >> 2];
               float x0, x1, x2, x3;
-              f2unpack(fma2(f2pack(__uint_as_float(sv[i + 0]), __uint_as_float(sv[i + 1])), sl2x2, f2pack(-l.x, -l.y)), x0, x1);
-              f2unpack(fma2(f2pack(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), sl2x2, f2pack(-l.z, -l.w)), x2, x3);
-              const uint64_t p01 = f2pack(fast_exp2(x0), fast_exp2(x1)), p23 = f2pack(fast_exp2(x2), fast_exp2(x3));
-              const uint64_t d01 = mul2(p01, sub2(f2pack(__uint_as_float(dv[i + 0]), __uint_as_float(dv[i + 1])), f2pack(dl.x, dl.y)));
-              const uint64_t d23 = mul2(p23, sub2(f2pack(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2pack(dl.z, dl.w)));
-              float a, b;
-              f2unpack(p01, a, b);
-              pp[(i >> 1) + 0] = pack_bf16x2(a, b);
-              f2unpack(p23, a, b);
-              pp[(i >> 1) + 1] = pack_bf16x2(a, b);
-              f2unpack(d01, a, b);
-              dd[(i >> 1) + 0] = pack_bf16x2(a, b);
-              f2unpack(d23, a, b);
-              dd[(i >> 1) + 1] = pack_bf16x2(a, b);
+              f2unpack(fma2(f2pack(__uint_as_float(sv[i >> 5][(i & 31) + 0]), __uint_as_float(sv[i >> 5][(i & 31) + 1])),
+                            sl2x2, f2pack(-l.x, -l.y)),
+                       x0, x1);
+              f2unpack(fma2(f2pack(__uint_as_float(sv[i >> 5][(i & 31) + 2]), __uint_as_float(sv[i >> 5][(i & 31) + 3])),
+                            sl2x2, f2pack(-l.z, -l.w)),
+                       x2, x3);
+              pf[i + 0] = fast_exp2(x0);
+              pf[i + 1] = fast_exp2(x1);
+              pf[i + 2] = fast_exp2(x2);
+              pf[i + 3] = fast_exp2(x3);
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 l = l4[i >> 2], dl = d4[i >> 2];
-              const float lv[4] = {l.x, l.y, l.z, l.w}, dd4[4] = {dl.x, dl.y, dl.z, dl.w};
-              float pv[4];
+            for (int i = 0; i < 64; i += 4) {
+              const float4 l = l4[i >> 2];
+              const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const int ie = (wg * 64 + c * 32 + i + e) & (tt - 1);
-                pv[e] = (ie >= i_lo && ie < i_hi) ? fast_exp2(fmaf(__uint_as_float(sv[i + e]), p.sl2, -lv[e])) : 0.f;
+                const int ie = (wg * 64 + i + e) & (tt - 1);
+                pf[i + e] = (ie >= i_lo && ie < i_hi)
+                                ? fast_exp2(fmaf(__uint_as_float(sv[i >> 5][(i & 31) + e]), p.sl2, -lv[e]))
+                                : 0.f;
               }
-              pp[(i >> 1) + 0] = pack_bf16x2(pv[0], pv[1]);
-              pp[(i >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
-              dd[(i >> 1) + 0] =
-                  pack_bf16x2(pv[0] * (__uint_as_float(dv[i + 0]) - dd4[0]), pv[1] * (__uint_as_float(dv[i + 1]) - dd4[1]));
-              dd[(i >> 1) + 1] =
-                  pack_bf16x2(pv[2] * (__uint_as_float(dv[i + 2]) - dd4[2]), pv[3] * (__uint_as_float(dv[i + 3]) - dd4[3]));
             }
           }
-          // P^T and dS^T as bf16 pairs over this half's columns, already read
-          tmem_st16(tmem + lb + K_T_S + wg * 64 + c * 16, pp);
-          tmem_st16(tmem + lb + K_T_DP + wg * 64 + c * 16, dd);
+          uint32_t pp[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pp[i] = pack_bf16x2(pf[2 * i], pf[2 * i + 1]);
+          tmem_st16(tmem + lb + K_T_S + wg * 64, *reinterpret_cast<const uint32_t(*)[16]>(&pp[0]));
+          tmem_st16(tmem + lb + K_T_S + wg * 64 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[16]));
+          tmem_wait_st();
         }
-        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KB_PDS_FULL + wg));
+        if (lane == 0) mbar_arrive(bar(KB_P_FULL));
+        // phase 2: dS^T = P^T (dP^T - D), as bf16 pairs over dP^T's columns
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_DP_FULL), qd_it & 1, abort))) { failed = true; break; }
+        tc_fence_after();
+        {
+          uint32_t dv[2][32];
+          tmem_ld32(tmem + lb + K_T_DP + wg * 64, dv[0]);
+          tmem_ld32(tmem + lb + K_T_DP + wg * 64 + 32, dv[1]);
+          tmem_wait_ld();
+          const float4* d4 = reinterpret_cast<const float4*>(rd + 128);  // D of the rows
+          uint32_t dd[32];
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            const float4 dl = d4[i >> 2];
+            const uint64_t d01 = mul2(f2pack(pf[i + 0], pf[i + 1]),
+                                      sub2(f2pack(__uint_as_float(dv[i >> 5][(i & 31) + 0]), __uint_as_float(dv[i >> 5][(i & 31) + 1])),
+                                           f2pack(dl.x, dl.y)));
+            const uint64_t d23 = mul2(f2pack(pf[i + 2], pf[i + 3]),
+                                      sub2(f2pack(__uint_as_float(dv[i >> 5][(i & 31) + 2]), __uint_as_float(dv[i >> 5][(i & 31) + 3])),
+                                           f2pack(dl.z, dl.w)));
+            float a, b;
+            f2unpack(d01, a, b);
+            dd[(i >> 1) + 0] = pack_bf16x2(a, b);
+            f2unpack(d23, a, b);
+            dd[(i >> 1) + 1] = pack_bf16x2(a, b);
+          }
+          tmem_st16(tmem + lb + K_T_DP + wg * 64, *reinterpret_cast<const uint32_t(*)[16]>(&dd[0]));
+          tmem_st16(tmem + lb + K_T_DP + wg * 64 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&dd[16]));
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KB_DS_FULL));
       }
       if (failed) break;
       // epilogue: this warpgroup's half of the key's dV and dK
