@@ -491,12 +491,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================ dK / dV pass
-// smem: K | V | (Q, dO) ring (2) | row data ring (2 x [lse2 128 | D 128]) | barriers
+// smem: K | V | (Q, dO) ring (2) | row data ring (4 x [lse2 128 | D 128]) | barriers
 constexpr int K_SM_K = 0;
 constexpr int K_SM_V = kTile;
 constexpr int K_SM_QD = 2 * kTile;          // stage s: Q at +s*2*kTile, dO at +kTile
 constexpr int K_SM_ROW = K_SM_QD + 4 * kTile;
-constexpr int K_SM_BAR = K_SM_ROW + 2 * 1024;
+constexpr int kRowSlots = 4;  // row data ring: tile i's slot was last read for tile i - 4
+constexpr int K_SM_BAR = K_SM_ROW + kRowSlots * 1024;
 constexpr int kDkvSmem = K_SM_BAR + 256 + 1024;
 constexpr uint32_t K_T_S = 0, K_T_DP = 128, K_T_DV = 256, K_T_DK = 384;
 // Per query tile i the MMA thread issues dP^T(i), dV(i) += P^T(i) dO(i),
@@ -636,19 +637,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (bool ok = true; ok; ok = q_next(p, q), ++qd_it) {
         const int st = qd_it & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_QD_EMPTY + st), ((qd_it >> 1) & 1) ^ 1, abort))) {
-          failed = true;
-          break;
-        }
         // LSE (log2 units) and D of the tile's rows; rows past the entry get
-        // LSE = +inf so that their probabilities vanish
-        float* rd = rowdata + st * 256;
+        // LSE = +inf so that their probabilities vanish.  Written before the
+        // wait for the Q / dO stage, so their loads overlap it: the slot was
+        // last read for tile qd_it - 4, whose stage this warp saw freed when
+        // it loaded tile qd_it - 2.
+        float* rd = rowdata + (qd_it % kRowSlots) * 256;
         for (int c = lane; c < 128; c += 32) {
           const int64_t tok = q.t0 + (c % tt);
           const int head = g * G + c / tt;
           const bool ok2 = tok < q.be.q_hi;
           rd[c] = ok2 ? p.lse[static_cast<int64_t>(head) * p.T + tok] * kLog2e : INFINITY;
           rd[128 + c] = ok2 ? p.delta[static_cast<int64_t>(head) * p.T + tok] : 0.f;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_QD_EMPTY + st), ((qd_it >> 1) & 1) ^ 1, abort))) {
+          failed = true;
+          break;
         }
         __syncwarp();
         if (lane == 0) {
@@ -797,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_S_FULL), qd_it & 1, abort))) { failed = true; break; }
         tc_fence_after();
-        const float* rd = rowdata + (qd_it & 1) * 256 + wg * 64;
+        const float* rd = rowdata + (qd_it % kRowSlots) * 256 + wg * 64;
         // row c (token t0 + c % tt) sees this key iff the token index i = c % tt
         // lies in [i_lo, i_hi)
         const bool key_ok = key >= q.be.k_lo && key < q.be.k_hi;
