@@ -491,41 +491,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================ dK / dV pass
-// smem: K | V | (Q, dO) ring (2) | row data ring (4 x [lse2 128 | D 128]) | barriers
+// smem: K | V | Q ring (3) | dO ring (2) | row data (lse2 128 | D 128) | barriers
 constexpr int K_SM_K = 0;
 constexpr int K_SM_V = kTile;
-constexpr int K_SM_QD = 2 * kTile;          // stage s: Q at +s*2*kTile, dO at +kTile
-constexpr int K_SM_ROW = K_SM_QD + 4 * kTile;
-constexpr int kRowSlots = 4;  // row data ring: tile i's slot was last read for tile i - 4
-constexpr int K_SM_BAR = K_SM_ROW + kRowSlots * 1024;
+// Q is read by S^T (early in a query tile's period) and by dK (late), dO by
+// dP^T and dV: a three-stage Q ring and a two-stage dO ring, so that the
+// next tile's Q has landed when its S^T is due.  One slot of row data (LSE,
+// D) fits beside them: the producer holds a tile's row data in registers
+// and writes it once the element-wise warps are done with the tile before.
+constexpr int kDkvQStages = 3, kDkvDoStages = 2;
+constexpr int K_SM_Q = 2 * kTile;
+constexpr int K_SM_DO = K_SM_Q + kDkvQStages * kTile;
+constexpr int K_SM_ROW = K_SM_DO + kDkvDoStages * kTile;
+constexpr int K_SM_BAR = K_SM_ROW + 1024;
 constexpr int kDkvSmem = K_SM_BAR + 256 + 1024;
 constexpr uint32_t K_T_S = 0, K_T_DP = 128, K_T_DV = 256, K_T_DK = 384;
-// Per query tile i the MMA thread issues dP^T(i), dV(i) += P^T(i) dO(i),
-// S^T(i+1) and, once dS^T(i) is in, dK(i) += dS^T(i) Q(i).  P^T(i) lives over
-// S^T(i)'s columns and dS^T(i) over dP^T(i)'s; S^T(i+1) is issued after dV(i)
-// and dP^T(i+1) after dK(i), and tensor operations run in issue order, so
-// each overwrites its columns only after they were read.  The element-wise
-// warps compute P^T(i) (phase 1, while dK(i-1) runs) and dS^T(i) (phase 2,
-// while dV(i) and S^T(i+1) run), keeping P in registers between the two.
+// Per query tile i the MMA thread issues dV(i) += P^T(i) dO(i), S^T(i+1),
+// dK(i) += dS^T(i) Q(i) once dS^T(i) is in, and dP^T(i+1) right behind it.
+// P^T(i) lives over S^T(i)'s columns and dS^T(i) over dP^T(i)'s; S^T(i+1) is
+// issued after dV(i) and dP^T(i+1) after dK(i), and tensor operations run in
+// issue order, so each overwrites its columns only after they were read.
+// The element-wise warps compute P^T(i) (phase 1) and dS^T(i) (phase 2),
+// keeping P in registers between the two; dP^T(i) is done by then.
 enum {
   KB_KV_FULL = 0,
   KB_KV_EMPTY = 1,
-  KB_QD_FULL = 2,   // +stage (2)
-  KB_QD_EMPTY = 4,  // +stage (2)
-  KB_S_FULL = 6,    // S^T of the tile is in TMEM
-  KB_P_FULL = 7,    // count 8: P^T of the tile is in TMEM
-  KB_DP_FULL = 8,   // dP^T of the tile is in TMEM
-  KB_DS_FULL = 9,   // count 8: dS^T of the tile is in TMEM
-  KB_ACC_DONE = 10,
-  KB_ACC_FREE = 11,   // count 8
-  KB_UNIT_FULL = 12,  // +slot (4): the unit ring's slot holds the next unit
-  KB_UNIT_EMPTY = 16, // +slot (4), count 9: the MMA thread and the element-wise warps read it
-  KB_N = 20
+  KB_Q_FULL = 2,    // +stage (3)
+  KB_Q_EMPTY = 5,   // +stage (3): the tile's dK has run
+  KB_DO_FULL = 8,   // +stage (2)
+  KB_DO_EMPTY = 10, // +stage (2): the tile's dV has run
+  KB_ROW_FULL = 12, // the tile's row data is in shared memory
+  KB_S_FULL = 13,   // S^T of the tile is in TMEM
+  KB_P_FULL = 14,   // count 8: P^T of the tile is in TMEM
+  KB_DP_FULL = 15,  // dP^T of the tile is in TMEM
+  KB_DS_FULL = 16,  // count 8: dS^T of the tile is in TMEM (also: its row data was read)
+  KB_ACC_DONE = 17,
+  KB_ACC_FREE = 18,   // count 8
+  KB_UNIT_FULL = 19,  // +slot (4): the unit ring's slot holds the next unit
+  KB_UNIT_EMPTY = 23, // +slot (4), count 9: the MMA thread and the element-wise warps read it
+  KB_N = 27
 };
 // The units (key tile, kv head) vary with how many query tiles see the key
 // tile; the ring sits after the barriers.
-constexpr int K_SM_URING = K_SM_BAR + 192;
-static_assert(KB_N * 8 + 8 <= 192, "dK/dV barrier area");
+constexpr int K_SM_URING = K_SM_BAR + 240;
+static_assert(KB_N * 8 + 8 <= 240, "dK/dV barrier area");
+static_assert(K_SM_BAR + 256 + 1024 <= 232448, "dK/dV shared memory");
 
 
 // Query tiles of a key tile: each entry's queries in steps of tile_tokens.
@@ -636,35 +646,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (bool ok = true; ok; ok = q_next(p, q), ++qd_it) {
-        const int st = qd_it & 1;
-        // LSE (log2 units) and D of the tile's rows; rows past the entry get
-        // LSE = +inf so that their probabilities vanish.  Written before the
-        // wait for the Q / dO stage, so their loads overlap it: the slot was
-        // last read for tile qd_it - 4, whose stage this warp saw freed when
-        // it loaded tile qd_it - 2.
-        float* rd = rowdata + (qd_it % kRowSlots) * 256;
-        for (int c = lane; c < 128; c += 32) {
+        const int qs = qd_it % kDkvQStages, ds = qd_it % kDkvDoStages;
+        // LSE (log2 units) and D of the tile's rows (lane takes rows lane +
+        // 32 k); rows past the entry get LSE = +inf so that their
+        // probabilities vanish
+        float lse4[4], d4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = lane + 32 * k;
           const int64_t tok = q.t0 + (c % tt);
           const int head = g * G + c / tt;
           const bool ok2 = tok < q.be.q_hi;
-          rd[c] = ok2 ? p.lse[static_cast<int64_t>(head) * p.T + tok] * kLog2e : INFINITY;
-          rd[128 + c] = ok2 ? p.delta[static_cast<int64_t>(head) * p.T + tok] : 0.f;
+          lse4[k] = ok2 ? p.lse[static_cast<int64_t>(head) * p.T + tok] * kLog2e : INFINITY;
+          d4[k] = ok2 ? p.delta[static_cast<int64_t>(head) * p.T + tok] : 0.f;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_QD_EMPTY + st), ((qd_it >> 1) & 1) ^ 1, abort))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_Q_EMPTY + qs), ((qd_it / kDkvQStages) & 1) ^ 1, abort))) {
           failed = true;
           break;
         }
-        __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(KB_QD_FULL + st), 2 * kTile);
-          const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile;
+          mbar_arrive_expect_tx(bar(KB_Q_FULL + qs), kTile);
           for (int hh = 0; hh < G; ++hh)
-            for (int h = 0; h < 2; ++h) {
-              tma_load_3d(qa + h * kHalf + hh * tt * 128, &tm_q, bar(KB_QD_FULL + st), h * 64, g * G + hh, q.t0);
-              tma_load_3d(qa + kTile + h * kHalf + hh * tt * 128, &tm_do, bar(KB_QD_FULL + st), h * 64, g * G + hh,
-                          q.t0);
-            }
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(sbase + K_SM_Q + qs * kTile + h * kHalf + hh * tt * 128, &tm_q, bar(KB_Q_FULL + qs), h * 64,
+                          g * G + hh, q.t0);
         }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_DO_EMPTY + ds), ((qd_it / kDkvDoStages) & 1) ^ 1, abort))) {
+          failed = true;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(KB_DO_FULL + ds), kTile);
+          for (int hh = 0; hh < G; ++hh)
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(sbase + K_SM_DO + ds * kTile + h * kHalf + hh * tt * 128, &tm_do, bar(KB_DO_FULL + ds),
+                          h * 64, g * G + hh, q.t0);
+        }
+        // the row slot is free once the element-wise warps are done with the
+        // tile before (its dS^T is in, after both of their phases read it)
+        if (qd_it > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(bar(KB_DS_FULL), (qd_it - 1) & 1, abort))) {
+          failed = true;
+          break;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          rowdata[lane + 32 * k] = lse4[k];
+          rowdata[128 + lane + 32 * k] = d4[k];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KB_ROW_FULL));
       }
       if (failed) break;
       u_next = publish();
@@ -685,21 +716,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       // base descriptors: K and V (K-major A), Q and dO of each stage as
       // K-major B (for S^T, dP^T) and as MN-major B (for dK, dV)
       const uint64_t d_k = sdesc_sw128(sbase + K_SM_K, 16, 1024), d_v = sdesc_sw128(sbase + K_SM_V, 16, 1024);
-      uint64_t d_q[2], d_do[2], d_qmn[2], d_domn[2];
-#pragma unroll
-      for (int st = 0; st < 2; ++st) {
-        const uint32_t qa = sbase + K_SM_QD + st * 2 * kTile;
-        d_q[st] = sdesc_sw128(qa, 16, 1024);
-        d_do[st] = sdesc_sw128(qa + kTile, 16, 1024);
-        d_qmn[st] = sdesc_sw128(qa, kHalf, 1024);
-        d_domn[st] = sdesc_sw128(qa + kTile, kHalf, 1024);
-      }
-      // S^T = K Q^T for the tile in stage st
-      auto issue_s = [&](int st) {
-        const uint64_t dq = st ? d_q[1] : d_q[0];
+      // descriptors of the Q stages (K-major B for S^T, MN-major B for dK) and
+      // of the dO stages (K-major for dP^T, MN-major for dV)
+      const uint32_t qa0 = sbase + K_SM_Q, da0 = sbase + K_SM_DO;
+      const uint64_t d_q0 = sdesc_sw128(qa0, 16, 1024), d_q1 = sdesc_sw128(qa0 + kTile, 16, 1024),
+                     d_q2 = sdesc_sw128(qa0 + 2 * kTile, 16, 1024);
+      const uint64_t d_qm0 = sdesc_sw128(qa0, kHalf, 1024), d_qm1 = sdesc_sw128(qa0 + kTile, kHalf, 1024),
+                     d_qm2 = sdesc_sw128(qa0 + 2 * kTile, kHalf, 1024);
+      const uint64_t d_do0 = sdesc_sw128(da0, 16, 1024), d_do1 = sdesc_sw128(da0 + kTile, 16, 1024);
+      const uint64_t d_dom0 = sdesc_sw128(da0, kHalf, 1024), d_dom1 = sdesc_sw128(da0 + kTile, kHalf, 1024);
+      // S^T = K Q^T for tile i (its Q landed)
+      auto issue_s = [&](uint32_t i) {
+        const uint32_t qs = i % kDkvQStages;
+        const uint64_t dq = qs == 0 ? d_q0 : (qs == 1 ? d_q1 : d_q2);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_bf16_ss(tmem + K_T_S, kmajor_step(d_k, kk), kmajor_step(dq, kk), id_kk, kk > 0);
         mma_commit(bar(KB_S_FULL));
+      };
+      // dP^T = V dO^T for tile i (its dO landed), over the columns of the
+      // previous tile's dS^T (read by its dK, issued earlier)
+      auto issue_dp = [&](uint32_t i) {
+        const uint64_t ddo = (i % kDkvDoStages) ? d_do1 : d_do0;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tmem + K_T_DP, kmajor_step(d_v, kk), kmajor_step(ddo, kk), id_kk, kk > 0);
+        mma_commit(bar(KB_DP_FULL));
+      };
+      auto wait_q = [&](uint32_t i) {
+        return mbar_wait_relaxed(bar(KB_Q_FULL + i % kDkvQStages), (i / kDkvQStages) & 1, abort);
+      };
+      auto wait_do = [&](uint32_t i) {
+        return mbar_wait_relaxed(bar(KB_DO_FULL + i % kDkvDoStages), (i / kDkvDoStages) & 1, abort);
       };
       uint32_t n_taken = 0;
       while (!failed) {
@@ -713,38 +760,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         QIter q;
         if (!q_begin(p, it, q)) continue;
         if (!mbar_wait_relaxed(bar(KB_KV_FULL), unit_it & 1, abort)) { failed = true; break; }
-        if (!mbar_wait_relaxed(bar(KB_QD_FULL + (qd_it & 1)), (qd_it >> 1) & 1, abort)) { failed = true; break; }
+        if (!wait_q(qd_it)) { failed = true; break; }
         tc_fence_after();
-        issue_s(qd_it & 1);
+        issue_s(qd_it);
+        if (!wait_do(qd_it)) { failed = true; break; }
+        tc_fence_after();
+        issue_dp(qd_it);
         bool first = true;
         for (bool ok = true; ok; ++qd_it) {
-          const int st = qd_it & 1;
-          const uint64_t dqm = st ? d_qmn[1] : d_qmn[0], ddom = st ? d_domn[1] : d_domn[0];
-          const uint64_t ddo = st ? d_do[1] : d_do[0];
+          const uint32_t qs = qd_it % kDkvQStages, ds = qd_it % kDkvDoStages;
+          const uint64_t dqm = qs == 0 ? d_qm0 : (qs == 1 ? d_qm1 : d_qm2), ddom = ds ? d_dom1 : d_dom0;
           const bool more = q_next(p, q);
           if (first && !mbar_wait_relaxed(bar(KB_ACC_FREE), (unit_it & 1) ^ 1, abort)) { failed = true; break; }
           if (!mbar_wait_relaxed(bar(KB_P_FULL), qd_it & 1, abort)) { failed = true; break; }
           tc_fence_after();
-          // dP^T = V dO^T over the columns of dS^T of the tile before (read
-          // by its dK, issued earlier)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + K_T_DP, kmajor_step(d_v, kk), kmajor_step(ddo, kk), id_kk, kk > 0);
-          mma_commit(bar(KB_DP_FULL));
           // dV += P^T dO (warpgroup h packed query rows 64h .. 64h + 63 into
           // columns 64h .. 64h + 31)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(tmem + K_T_DV, tmem + K_T_S + (kk >> 2) * 64 + (kk & 3) * 8, mnmajor_step(ddom, kk), id_mn,
                         (!first || kk > 0) ? 1u : 0u);
+          mma_commit(bar(KB_DO_EMPTY + ds));  // dP^T and dV have read dO
           // The next tile's S^T over the columns dV has just read: now, so
           // that it runs while the element-wise warps compute dS^T, when its
           // Q has landed; otherwise after dK, so as not to hold dK up.
-          const uint32_t nb = KB_QD_FULL + ((qd_it + 1) & 1), nph = ((qd_it + 1) >> 1) & 1;
+          const uint32_t nb = KB_Q_FULL + (qd_it + 1) % kDkvQStages, nph = ((qd_it + 1) / kDkvQStages) & 1;
           const bool s_early = more && mbar_test_wait(bar(nb), nph);
           if (s_early) {
             tc_fence_after();
-            issue_s((qd_it + 1) & 1);
+            issue_s(qd_it + 1);
           }
           if (!mbar_wait_relaxed(bar(KB_DS_FULL), qd_it & 1, abort)) { failed = true; break; }
           tc_fence_after();
@@ -753,14 +797,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(tmem + K_T_DK, tmem + K_T_DP + (kk >> 2) * 64 + (kk & 3) * 8, mnmajor_step(dqm, kk), id_mn,
                         (!first || kk > 0) ? 1u : 0u);
-          mma_commit(bar(KB_QD_EMPTY + st));
-          if (more && !s_early) {
-            if (!mbar_wait_relaxed(bar(nb), nph, abort)) {
+          mma_commit(bar(KB_Q_EMPTY + qs));  // S^T and dK have read Q
+          if (more) {
+            if (!s_early) {
+              if (!mbar_wait_relaxed(bar(nb), nph, abort)) {
+                failed = true;
+                break;
+              }
+              tc_fence_after();
+              issue_s(qd_it + 1);
+            }
+            // the next tile's dP^T right behind dK: the element-wise warps
+            // find it done when they reach its dS^T
+            if (!wait_do(qd_it + 1)) {
               failed = true;
               break;
             }
             tc_fence_after();
-            issue_s((qd_it + 1) & 1);
+            issue_dp(qd_it + 1);
           }
           first = false;
           ok = more;
@@ -794,14 +848,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!q_begin(p, it, q)) continue;
       const int32_t key = it.k_start + r;
       for (bool ok = true; ok; ok = q_next(p, q), ++qd_it, ++g_it) {
-        // the row data was written by the producer before it armed QD_FULL
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_QD_FULL + (qd_it & 1)), (qd_it >> 1) & 1, abort))) {
+        // the tile's row data (the producer writes it once this warp's
+        // previous tile is done)
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_ROW_FULL), qd_it & 1, abort))) {
           failed = true;
           break;
         }
         if (!__all_sync(0xffffffffu, mbar_wait(bar(KB_S_FULL), qd_it & 1, abort))) { failed = true; break; }
         tc_fence_after();
-        const float* rd = rowdata + (qd_it % kRowSlots) * 256 + wg * 64;
+        const float* rd = rowdata + wg * 64;
         // row c (token t0 + c % tt) sees this key iff the token index i = c % tt
         // lies in [i_lo, i_hi)
         const bool key_ok = key >= q.be.k_lo && key < q.be.k_hi;
