@@ -549,6 +549,21 @@ def main() -> int:
         "gpu_launches": ((1 if dec._plan.fused() else 2) + (2 if acc is not None else 0) + 1 + 3) * K,
         "clocks": clk,
     }
+    if dec._plan.fused():
+        # the step is one kernel (the prefix pass call launches nothing)
+        fused_gbs = all_b / (t_dec * 1e-3) / 1e9
+        pre_units = sum(max(p.branch_prefix_len or [0]) for p in dw.pages)
+        line["roofline"] = {"bound": "hbm", "kernel": "attn_tc_kernel<MODE_VERIFY>", "achieved": fused_gbs, "peak": hbm,
+                            "unit": "GB/s", "frac": fused_gbs / hbm, "peak_source": peak_src,
+                            "traffic": traffic_for("verify_fused", own_units + pre_units), "algorithmic_bytes": all_b,
+                            "ms": t_dec}
+        del line["kernels"]["prefix_pass"], line["kernels"]["own_pass"]
+        line["kernels"]["fused_pass"] = {"ms": t_dec, "achieved_gbs": fused_gbs, "frac_hbm": fused_gbs / hbm,
+                                         "algorithmic_bytes": all_b, "algorithmic_flops": dec_fl,
+                                         "achieved_tflops": dec_fl / (t_dec * 1e-3) / 1e12}
+        line["config"]["step"] = ("value and ms_per_step cover the decode step (one fused verify pass); the forward "
+                                  "and its backward run in the same timed loop and are reported under 'forward' and "
+                                  "'backward'")
     if acc is not None:
         acc_gbs = acc.bytes / (t_acc * 1e-3) / 1e9
         line["kernels"]["accept"] = {
