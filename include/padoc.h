@@ -236,7 +236,10 @@ PADOC_API int padoc_tree_desc_bwd_plan(const padoc_tree_desc* desc, int32_t* ite
  * its draft-tree ancestors and itself (HSD page, "prefix-tree batching";
  * HPD-Parsing: parallel verify of drafted tokens on forked branches).
  * The shared prefix of a page is streamed from HBM once for all branches of
- * the page (cascade); partial softmaxes are merged by log-sum-exp.
+ * the page (cascade); partial softmaxes are merged by log-sum-exp.  A verify
+ * step whose pages each fit one prefix chunk (see padoc_decode_plan_fused)
+ * runs as one kernel that walks, per row tile, the prefix, the own suffixes
+ * and the query block in a single running softmax.
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t n_pages;
