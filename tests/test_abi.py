@@ -258,6 +258,16 @@ def test_backward_plan_covers_every_pair_once(padoc_lib, seed, order):
     assert np.array_equal(got, want)
 
 
+def test_backward_plan_key_tiles_in_position_order(padoc_lib):
+    """The key-stationary units stay in position order (the kernel draws them
+    in order, so CTAs at work together hold key tiles of one page and share
+    its queries' Q and dO in L2); every key tile with a query appears once."""
+    w = wl.random_pages(7, n_pages=4, max_prefix=400, max_regions=5, max_layout=40, max_content=200)
+    items, _ = padoc.TreeDesc(w.pages, padoc.PACK_CANONICAL).bwd_plan()
+    starts = [int(it[0]) for it in items]
+    assert starts == sorted(starts) and len(set(starts)) == len(starts)
+
+
 def _verify_plan(Hq, prefix, q_len, n_branches=3, own=40):
     """A host-only plan of one page: `prefix` tokens shared by n_branches
     forks with `own` tokens each and `q_len` query rows per branch."""
