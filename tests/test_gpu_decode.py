@@ -45,10 +45,10 @@ def test_small_decode_groups(harness, G):
     check(og, lg, O, L, "bf16", f"decode G={G}")
 
 
-@pytest.mark.parametrize("G", [1, 4])
+@pytest.mark.parametrize("G", [1, 4, 8])
 def test_small_verify_groups(harness, G):
-    """Draft trees with G = 1 (keys-on-M own pass, 16 rows per unit) and
-    G = 4 (the rows-on-M tensor-core own pass)."""
+    """Draft trees with G = 1 (two passes, keys-on-M own pass) and G = 4 and
+    8 (the fused pass; at G = 8 a row tile holds 16 query tokens)."""
     w = wl.small_decode(40 + G, n_pages=3, max_prefix=500, max_branches=5, max_own=300, Hq=2 * G, Hkv=2)
     og, lg, O, L = _decode(harness, w, 40 + G)
     check(og, lg, O, L, "bf16", f"verify G={G}")
