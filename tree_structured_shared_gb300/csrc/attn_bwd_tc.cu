@@ -128,15 +128,13 @@ constexpr uint32_t Q_T_S = 0, Q_T_DP = 128, Q_T_DS = 256, Q_T_DQ = 384;
 enum {
   QB_QD_FULL = 0,
   QB_QD_EMPTY = 1,
-  QB_K_FULL = 2,    // +stage (3)
+  QB_K_FULL = 2,    // +K stage (3): K and V of the tile have landed
   QB_K_EMPTY = 5,   // +stage (3): the tile's dQ has run
-  QB_V_FULL = 8,    // +stage (2)
   QB_V_EMPTY = 10,  // +stage (2): the tile's dP has run
   QB_SP_FULL = 12,  // S and dP of the tile are in TMEM
   QB_RD = 13,       // count 8: both warpgroups have read them (the columns are free)
-  // per key half h (columns 64h .. 64h + 63 of S and dP, warpgroup h):
-  QB_DS_FULL = 14,  // +h, count 4: dS of the half is in TMEM
-  QB_DQ_DONE = 16,  // +h: dQ += dS K over the half has run (the dS columns are free)
+  QB_DS_FULL = 14,  // count 8: dS of the tile is in TMEM (both warpgroups)
+  QB_DQ_DONE = 16,  // dQ += dS K of the tile has run (the dS columns are free)
   QB_DQ_ALL = 18,   // the unit's dQ is complete
   QB_ACC_FREE = 19,  // count 8: the epilogue has read dQ
   QB_UNIT_FULL = 20,   // +slot (4): the unit ring's slot holds the next unit
@@ -222,10 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_N; ++i)
-      mbar_init(bar(i), (i == QB_DS_FULL || i == QB_DS_FULL + 1)
-                            ? 4u
-                            : ((i == QB_ACC_FREE || i == QB_RD) ? 8u
-                                                                : ((i >= QB_UNIT_EMPTY && i < QB_UNIT_EMPTY + kURing) ? 9u : 1u)));
+      mbar_init(bar(i), (i == QB_DS_FULL || i == QB_ACC_FREE || i == QB_RD)
+                            ? 8u
+                            : ((i >= QB_UNIT_EMPTY && i < QB_UNIT_EMPTY + kURing) ? 9u : 1u));
     *abort = 0;
     fence_mbar_init();
   }
@@ -282,14 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         KeyIter t;
         for (bool ok = key_begin(p, w, t); ok; ok = key_next(p, w, t), ++kv_it) {
           const int ks = kv_it % kDqKStages, vs = kv_it % kDqVStages;
+          // K and V of a tile land on one barrier (one wait for the MMA
+          // thread); a V stage frees (after dP) before the K stage of the
+          // same tile (after dQ of the tile before)
           if (!mbar_wait(bar(QB_K_EMPTY + ks), ((kv_it / kDqKStages) & 1) ^ 1, abort)) { failed = true; break; }
-          mbar_arrive_expect_tx(bar(QB_K_FULL + ks), kTile);
+          if (!mbar_wait(bar(QB_V_EMPTY + vs), ((kv_it / kDqVStages) & 1) ^ 1, abort)) { failed = true; break; }
+          mbar_arrive_expect_tx(bar(QB_K_FULL + ks), 2 * kTile);
           for (int h = 0; h < 2; ++h)
             tma_load_3d(sbase + Q_SM_K + ks * kTile + h * kHalf, &tm_k, bar(QB_K_FULL + ks), h * 64, w.g, t.ks);
-          if (!mbar_wait(bar(QB_V_EMPTY + vs), ((kv_it / kDqVStages) & 1) ^ 1, abort)) { failed = true; break; }
-          mbar_arrive_expect_tx(bar(QB_V_FULL + vs), kTile);
           for (int h = 0; h < 2; ++h)
-            tma_load_3d(sbase + Q_SM_V + vs * kTile + h * kHalf, &tm_v, bar(QB_V_FULL + vs), h * 64, w.g, t.ks);
+            tma_load_3d(sbase + Q_SM_V + vs * kTile + h * kHalf, &tm_v, bar(QB_K_FULL + ks), h * 64, w.g, t.ks);
         }
         if (failed) break;
         u_next = publish();
@@ -318,21 +317,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t d_kmn2 = sdesc_sw128(sbase + Q_SM_K + 2 * kTile, kHalf, 1024);
       auto issue_dq = [&](uint32_t tile_it, bool first, bool last) -> bool {
         // dQ += dS K for tile tile_it (dS in TMEM, K of its stage as MN-major
-        // B), one key half at a time as each warpgroup finishes its dS
+        // B).  One wait and one commit for the whole tile: every wait, fence
+        // and commit between MMA groups leaves the pipe idle once the few
+        // queued MMAs have run, and both warpgroups finish dS together.
         if (first && !mbar_wait_relaxed(bar(QB_ACC_FREE), (unit_it & 1) ^ 1, abort)) return false;
         const int st = tile_it % kDqKStages;
         const uint64_t kd = st == 0 ? d_kmn0 : (st == 1 ? d_kmn1 : d_kmn2);
-        for (int half = 0; half < 2; ++half) {
-          if (!mbar_wait_relaxed(bar(QB_DS_FULL + half), tile_it & 1, abort)) return false;
-          tc_fence_after();
+        if (!mbar_wait_relaxed(bar(QB_DS_FULL), tile_it & 1, abort)) return false;
+        tc_fence_after();
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int kk = half * 4 + k4;
-            mma_bf16_ts(tmem + Q_T_DQ, tmem + Q_T_DS + kk * 8, mnmajor_step(kd, kk), id_mn,
-                        (!first || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(QB_DQ_DONE + half));
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + Q_T_DQ, tmem + Q_T_DS + kk * 8, mnmajor_step(kd, kk), id_mn,
+                      (!first || kk > 0) ? 1u : 0u);
+        mma_commit(bar(QB_DQ_DONE));
         mma_commit(bar(QB_K_EMPTY + st));
         if (last) mma_commit(bar(QB_DQ_ALL));
         return true;
@@ -352,7 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n; ++j, ++kv_it, ++g_it) {
           const int ks = kv_it % kDqKStages, vs = kv_it % kDqVStages;
           if (!mbar_wait_relaxed(bar(QB_K_FULL + ks), (kv_it / kDqKStages) & 1, abort)) { failed = true; break; }
-          if (!mbar_wait_relaxed(bar(QB_V_FULL + vs), (kv_it / kDqVStages) & 1, abort)) { failed = true; break; }
           const uint64_t dk = ks == 0 ? d_k0 : (ks == 1 ? d_k1 : d_k2), dv = vs ? d_v1 : d_v0;
           // S and dP go over columns both warpgroups have read (they compute the
           // previous tile's dS from registers meanwhile)
@@ -449,14 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // dS goes over the previous tile's dS once that tile's dQ has read it
         if (g_it > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_DQ_DONE + wg), (g_it - 1) & 1, abort))) { failed = true; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(QB_DQ_DONE), (g_it - 1) & 1, abort))) { failed = true; break; }
           tc_fence_after();
         }
         tmem_st32(tmem + lb + Q_T_DS + wg * 32, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(QB_DS_FULL + wg));
+        if (lane == 0) mbar_arrive(bar(QB_DS_FULL));
       }
       if (failed) break;
       // epilogue: this warpgroup's half of the row's dQ
