@@ -112,7 +112,7 @@ __device__ __forceinline__ bool take_unit(uint32_t& k, int& u, volatile int32_t*
 }
 
 // ============================================================ dQ pass
-// smem: Q | dO | K ring (2) | V ring (2) | barriers
+// smem: Q | dO | K ring (3) | V ring (2) | barriers
 constexpr int Q_SM_Q = 0;
 constexpr int Q_SM_DO = kTile;
 // K is read by S (early in a tile's period) and by dQ (late), V only by dP:
@@ -139,7 +139,7 @@ enum {
   QB_ACC_FREE = 19,  // count 8: the epilogue has read dQ
   QB_UNIT_FULL = 20,   // +slot (4): the unit ring's slot holds the next unit
   QB_UNIT_EMPTY = 24,  // +slot (4), count 9: the MMA thread and the element-wise warps read it
-  QB_N = 28
+  QB_N = 28  // slots 8-9, 15 and 17 are unused
 };
 constexpr int Q_SM_URING = Q_SM_BAR + 240;
 static_assert(QB_N * 8 + 8 <= 240, "dQ barrier area");
